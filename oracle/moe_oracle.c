@@ -1,0 +1,478 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for the DeepSeek-V3-style MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this file;
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use it.  It shares
+ * no code, header, table or constant generator with the CUDA library.
+ *
+ * Sources (cited by page title and section):
+ *  [P1] "从 1024 块 GPU 到 558 万美元：拆解 DeepSeek-V3 的算法-系统协同设计" (wsisp.com)
+ *       §2.2 MoEGate listing (sigmoid gate, selection-only bias, group-limited top-k,
+ *       weights from un-biased scores, normalisation, routed_scaling_factor);
+ *       §2.3 dispatch skeleton (per-expert counts, argsort of the flat expert ids);
+ *       §5.1 blockwise FP8 GEMM sketch (FP8 operands, per-block scales applied during
+ *       accumulation, FP32 accumulation, output quantised as needed).
+ *  [P2] "深入理解 DeepSeek-V3" -- Chinese précis of "Insights into DeepSeek-V3: Scaling
+ *       Challenges and Reflections on Hardware for AI Architectures" (arXiv 2505.09343)
+ *       §3.1 (8 routed + 1 shared expert per token; FP8 dispatch, BF16 combine);
+ *       §3.2 (activations quantised in 1x128 tiles, weights in 128x128 blocks, each with
+ *       a scale; FP32 accumulation requested).
+ *  [OFP8] OCP "8-bit Floating Point Specification (OFP8)" rev 1.0, E4M3 encoding table.
+ *
+ * Readings of the pages where they are silent (each also listed in the design notes):
+ *  - experts outside the kept groups are masked with -inf (the listing writes 0.0; the two
+ *    agree whenever every selection score is positive);
+ *  - ties in every top-k go to the lower index; slots are in descending selection score;
+ *  - a block scale is amax/448 in FP32 (amax == 0 gives scale 1 and all-zero codes), and
+ *    values are encoded as e4m3(v * (448/amax)) with round-to-nearest-even and saturation;
+ *  - the expert FFN is SwiGLU: down(silu(gate(x)) * up(x)), no biases, gate rows 0..I-1
+ *    and up rows I..2I-1 of the stacked first weight;
+ *  - h goes from FP32 straight to FP8 1x128 tiles; expert outputs are BF16 and unweighted;
+ *    the combine weights them in FP32 in slot order, adds the shared expert, rounds once;
+ *  - the load-driven bias update is b_i += 1e-3 * sign(mean_load - load_i).
+ *
+ * Arithmetic: dot products accumulate in double and are rounded to float once, so the
+ * oracle is the exact result up to that final rounding.  Products of two E4M3 values are
+ * exact in double and a 128-term block sum of them is exact in double too.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------------------ */
+/* number formats                                                                        */
+/* ------------------------------------------------------------------------------------ */
+
+/* BF16 -> FP32 is exact: the BF16 bits are the upper half of the FP32 bits. */
+float orc_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* FP32 -> BF16, round to nearest, ties to even (the IEEE default rounding). */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* NaN */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* [OFP8] E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent field 0
+ * holds the subnormals m * 2^-9; S.1111.111 is NaN; there is no infinity, so the
+ * largest finite magnitude is S.1111.110 = 1.75 * 2^8 = 448. */
+double orc_e4m3_to_double(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Magnitude of the non-negative finite code c (0..126), increasing in c. */
+static double e4m3_mag(int c) { return orc_e4m3_to_double((uint8_t)c); }
+
+/* FP32 -> E4M3 by the definition of round-to-nearest-even with saturation to the largest
+ * finite value: pick the representable magnitude nearest to |v|; on an exact tie pick the
+ * code whose last bit is 0.  Magnitudes at or above 448 (including infinity) give 448.
+ * NaN gives S.1111.111. */
+uint8_t orc_f32_to_e4m3(float v)
+{
+    if (isnan(v)) return 0x7f;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7e;
+    int lo = 0, hi = 126; /* largest code whose magnitude is <= a */
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (e4m3_mag(mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    double dlo = a - e4m3_mag(lo), dhi = e4m3_mag(lo + 1) - a; /* both exact in double */
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = lo + 1;
+    else c = (lo & 1) ? lo + 1 : lo;
+    return sign | (uint8_t)c;
+}
+
+/* Element i of an input array that is FP32 (is_bf16 == 0) or BF16 (is_bf16 != 0). */
+static inline float load_elem(const void* p, int is_bf16, int64_t i)
+{
+    return is_bf16 ? orc_bf16_to_f32(((const uint16_t*)p)[i]) : ((const float*)p)[i];
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P2 §3.2] fine-grained quantisation                                                   */
+/* ------------------------------------------------------------------------------------ */
+
+/* Encode one tile of n values (v[i*stride]) given its amax; writes codes and returns the
+ * FP32 scale.  scale = amax/448; codes = e4m3(v * (448/amax)); amax == 0 -> scale 1. */
+static float quant_tile(float amax, const void* src, int64_t base, int is_bf16, int64_t n,
+                        int64_t stride, uint8_t* dst, int64_t dbase, int64_t dstride)
+{
+    if (amax == 0.0f) {
+        for (int64_t i = 0; i < n; ++i) dst[dbase + i * dstride] = 0;
+        return 1.0f;
+    }
+    float mul = 448.0f / amax;
+    for (int64_t i = 0; i < n; ++i) {
+        float v = load_elem(src, is_bf16, base + i * stride);
+        dst[dbase + i * dstride] = orc_f32_to_e4m3(v * mul);
+    }
+    return amax / 448.0f;
+}
+
+/* Activations: one scale per row per 128 consecutive columns.
+ * x [rows, cols] (cols % 128 == 0) -> q [rows, cols] E4M3 codes, s [rows, cols/128]. */
+void orc_quant_1x128(int64_t rows, int64_t cols, const void* x, int x_is_bf16,
+                     uint8_t* q, float* s)
+{
+    int64_t nb = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            int64_t base = r * cols + b * 128;
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i) {
+                float a = fabsf(load_elem(x, x_is_bf16, base + i));
+                if (a > amax) amax = a;
+            }
+            s[r * nb + b] = quant_tile(amax, x, base, x_is_bf16, 128, 1, q, base, 1);
+        }
+    }
+}
+
+/* Weights: one scale per 128x128 block of each matrix.
+ * w [n_mats, rows, cols] (rows, cols % 128 == 0) -> q same shape, s [n_mats, rows/128, cols/128]. */
+void orc_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const void* w, int w_is_bf16,
+                       uint8_t* q, float* s)
+{
+    int64_t rb = rows / 128, cb = cols / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < n_mats; ++m) {
+        for (int64_t i = 0; i < rb; ++i) {
+            for (int64_t j = 0; j < cb; ++j) {
+                int64_t base = m * rows * cols + i * 128 * cols + j * 128;
+                float amax = 0.0f;
+                for (int64_t r = 0; r < 128; ++r)
+                    for (int64_t c = 0; c < 128; ++c) {
+                        float a = fabsf(load_elem(w, w_is_bf16, base + r * cols + c));
+                        if (a > amax) amax = a;
+                    }
+                float scale = 1.0f;
+                for (int64_t r = 0; r < 128; ++r)
+                    scale = quant_tile(amax, w, base + r * cols, w_is_bf16, 128, 1, q,
+                                       base + r * cols, 1);
+                s[(m * rb + i) * cb + j] = scale;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1 §2.2] MoEGate                                                                     */
+/* ------------------------------------------------------------------------------------ */
+
+/* For every token: logits = x . Wg^T (accumulated in double, rounded to float), scores =
+ * sigmoid(logits), selection scores c = scores + bias; group score = sum of the two largest
+ * c in the group; keep the topk_group groups with the largest group scores; among experts
+ * in kept groups take the top_k largest c; weights = scores at those experts, divided by
+ * (their sum + 1e-20) when top_k > 1, then multiplied by routed_scaling_factor.
+ *
+ * x [T,H], Wg [E,H] (FP32 or BF16); bias [E].  Outputs: topk_idx/topk_w [T,K] in
+ * descending-c slot order; scores_out [T,E] (may be NULL); margin [T] (may be NULL) =
+ * min over the group cut (TG-th vs best dropped group score) and the expert cut (K-th vs
+ * best unselected candidate c); +inf where a cut does not exist. */
+void orc_gate(int64_t T, int H, int E, int G, int TG, int K, float rsf,
+              const void* x, int x_is_bf16, const void* Wg, int w_is_bf16, const float* bias,
+              int32_t* topk_idx, float* topk_w, float* scores_out, float* margin)
+{
+    int gsz = E / G;
+#pragma omp parallel
+    {
+        float* s = (float*)malloc(sizeof(float) * E);
+        float* c = (float*)malloc(sizeof(float) * E);
+        float* gs = (float*)malloc(sizeof(float) * G);
+        char* gkeep = (char*)malloc(G);
+        char* taken = (char*)malloc(E);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t t = 0; t < T; ++t) {
+            /* logits and sigmoid scores */
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h)
+                    acc += (double)load_elem(x, x_is_bf16, t * H + h) *
+                           (double)load_elem(Wg, w_is_bf16, (int64_t)e * H + h);
+                float logit = (float)acc;
+                s[e] = (float)(1.0 / (1.0 + exp(-(double)logit)));
+                c[e] = s[e] + bias[e];
+            }
+            if (scores_out)
+                for (int e = 0; e < E; ++e) scores_out[t * E + e] = s[e];
+            /* group scores: sum of the two largest selection scores of each group */
+            for (int g = 0; g < G; ++g) {
+                float b1 = -INFINITY, b2 = -INFINITY;
+                for (int j = 0; j < gsz; ++j) {
+                    float v = c[g * gsz + j];
+                    if (v > b1) { b2 = b1; b1 = v; }
+                    else if (v > b2) b2 = v;
+                }
+                gs[g] = b1 + b2;
+                gkeep[g] = 0;
+            }
+            /* keep topk_group groups: repeated arg-max, ties to the lower group index */
+            float last_kept_gs = INFINITY;
+            for (int r = 0; r < TG; ++r) {
+                int best = -1;
+                for (int g = 0; g < G; ++g)
+                    if (!gkeep[g] && (best < 0 || gs[g] > gs[best])) best = g;
+                gkeep[best] = 1;
+                last_kept_gs = gs[best];
+            }
+            float best_dropped_gs = -INFINITY;
+            for (int g = 0; g < G; ++g)
+                if (!gkeep[g] && gs[g] > best_dropped_gs) best_dropped_gs = gs[g];
+            /* top_k experts among kept groups (masked experts count as -inf) */
+            for (int e = 0; e < E; ++e) taken[e] = 0;
+            float last_c = INFINITY;
+            for (int k = 0; k < K; ++k) {
+                int best = -1;
+                for (int e = 0; e < E; ++e) {
+                    if (taken[e] || !gkeep[e / gsz]) continue;
+                    if (best < 0 || c[e] > c[best]) best = e;
+                }
+                taken[best] = 1;
+                topk_idx[t * K + k] = best;
+                last_c = c[best];
+            }
+            float best_unsel_c = -INFINITY;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && gkeep[e / gsz] && c[e] > best_unsel_c) best_unsel_c = c[e];
+            if (margin) {
+                float mg = (TG < G) ? last_kept_gs - best_dropped_gs : INFINITY;
+                float me = last_c - best_unsel_c;
+                margin[t] = mg < me ? mg : me;
+            }
+            /* weights from the un-biased scores */
+            float w[1024];
+            for (int k = 0; k < K; ++k) w[k] = s[topk_idx[t * K + k]];
+            if (K > 1) {
+                float den = 0.0f;
+                for (int k = 0; k < K; ++k) den = den + w[k];
+                den = den + 1e-20f;
+                for (int k = 0; k < K; ++k) w[k] = w[k] / den;
+            }
+            for (int k = 0; k < K; ++k) topk_w[t * K + k] = w[k] * rsf;
+        }
+        free(s); free(c); free(gs); free(gkeep); free(taken);
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1 §2.3] counts and permutation by expert                                            */
+/* ------------------------------------------------------------------------------------ */
+
+/* counts[e] = number of (token, slot) pairs routed to e.  Rows are ordered expert-major and,
+ * within an expert, by ascending token index (the stable argsort of the flat expert ids).
+ * With has_shared, slot group E holds every token once, in order, after the routed rows.
+ * offs [E+1+has_shared] is the exclusive prefix sum; perm_tok[row] is the token of a row;
+ * row_of[t*K+k] is the row of (t, k). */
+void orc_permute(int64_t T, int E, int K, int has_shared, const int32_t* topk_idx,
+                 int32_t* counts, int32_t* offs, int32_t* perm_tok, int32_t* row_of)
+{
+    int64_t* fill = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t i = 0; i < T * K; ++i) counts[topk_idx[i]] += 1;
+    offs[0] = 0;
+    for (int e = 0; e < E; ++e) offs[e + 1] = offs[e] + counts[e];
+    if (has_shared) offs[E + 1] = offs[E] + (int32_t)T;
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[t * K + k];
+            int64_t pos = offs[e] + fill[e]++;
+            perm_tok[pos] = (int32_t)t;
+            row_of[t * K + k] = (int32_t)pos;
+        }
+    if (has_shared)
+        for (int64_t t = 0; t < T; ++t) perm_tok[offs[E] + t] = (int32_t)t;
+    free(fill);
+}
+
+/* load-driven bias update: b_i += 1e-3 * sign(mean_load - load_i), mean_load = T*K/E.
+ * The sign is taken in integers: sign(T*K - E*load_i). */
+void orc_bias_update(int E, int64_t T, int K, const int32_t* counts, float* bias)
+{
+    for (int e = 0; e < E; ++e) {
+        int64_t d = T * (int64_t)K - (int64_t)E * (int64_t)counts[e];
+        int sgn = (d > 0) - (d < 0);
+        bias[e] = bias[e] + 1e-3f * (float)sgn;
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1 §5.1][P2 §3.2] routed / shared SwiGLU expert with blockwise FP8 operands          */
+/* ------------------------------------------------------------------------------------ */
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* One dot product of a 1x128-scaled activation row with a 128x128-scaled weight row:
+ * sum_kb (sa[kb]*sb[kb]) * sum_{k in kb} dq(a_k)*dq(w_k), in double. */
+static double block_dot(int K, const double* a_dq, const float* a_s, const uint8_t* w,
+                        const float* w_s, const double* lut)
+{
+    double acc = 0.0;
+    for (int kb = 0; kb < K / 128; ++kb) {
+        double p = 0.0;
+        for (int k = kb * 128; k < kb * 128 + 128; ++k) p += a_dq[k] * lut[w[k]];
+        acc += ((double)a_s[kb] * (double)w_s[kb]) * p;
+    }
+    return acc;
+}
+
+/* rows x [n_rows] each through expert row_expert[r]:
+ *   g_j = <x, W13[e, j]>, u_j = <x, W13[e, I + j]>      (1x128 x 128x128 blockwise, FP32 result)
+ *   h_j = silu(g_j) * u_j                                (in double, rounded to FP32)
+ *   hq, hs = 1x128 quantisation of h
+ *   y_n = <hq, W2[e, n]>                                 (blockwise, rounded to BF16)
+ * aq [n_rows, H] codes, as [n_rows, H/128]; W13 [nE, 2I, H], W13s [nE, 2I/128, H/128];
+ * W2 [nE, H, I], W2s [nE, H/128, I/128].  gu_out [n_rows, 2I] (g then u, FP32),
+ * h_out [n_rows, I] (FP32), hq_out/hs_out: each may be NULL; y_out [n_rows, H] BF16 bits. */
+void orc_ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* as,
+                 const int32_t* row_expert, const uint8_t* W13, const float* W13s,
+                 const uint8_t* W2, const float* W2s, float* gu_out, float* h_out,
+                 uint8_t* hq_out, float* hs_out, uint16_t* y_out)
+{
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = orc_e4m3_to_double((uint8_t)c);
+    int hb = H / 128, ib = I / 128;
+#pragma omp parallel
+    {
+        double* a_dq = (double*)malloc(sizeof(double) * H);
+        double* h_dq = (double*)malloc(sizeof(double) * I);
+        float* h = (float*)malloc(sizeof(float) * I);
+        uint8_t* hq = (uint8_t*)malloc(I);
+        float* hs = (float*)malloc(sizeof(float) * ib);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int64_t e = row_expert[r];
+            const uint8_t* w13 = W13 + e * (int64_t)(2 * I) * H;
+            const float* w13s = W13s + e * (int64_t)(2 * I / 128) * hb;
+            const uint8_t* w2 = W2 + e * (int64_t)H * I;
+            const float* w2s = W2s + e * (int64_t)hb * ib;
+            for (int k = 0; k < H; ++k) a_dq[k] = lut[aq[r * H + k]];
+            const float* sa = as + r * hb;
+            for (int j = 0; j < I; ++j) {
+                float g = (float)block_dot(H, a_dq, sa, w13 + (int64_t)j * H,
+                                           w13s + (int64_t)(j / 128) * hb, lut);
+                float u = (float)block_dot(H, a_dq, sa, w13 + (int64_t)(I + j) * H,
+                                           w13s + (int64_t)((I + j) / 128) * hb, lut);
+                h[j] = (float)(silu((double)g) * (double)u);
+                if (gu_out) {
+                    gu_out[r * 2 * I + j] = g;
+                    gu_out[r * 2 * I + I + j] = u;
+                }
+            }
+            orc_quant_1x128(1, I, h, 0, hq, hs);
+            for (int k = 0; k < I; ++k) h_dq[k] = lut[hq[k]];
+            for (int n = 0; n < H; ++n) {
+                float y = (float)block_dot(I, h_dq, hs, w2 + (int64_t)n * I,
+                                           w2s + (int64_t)(n / 128) * ib, lut);
+                y_out[r * H + n] = orc_f32_to_bf16(y);
+            }
+            if (h_out) memcpy(h_out + r * I, h, sizeof(float) * I);
+            if (hq_out) memcpy(hq_out + r * I, hq, I);
+            if (hs_out) memcpy(hs_out + r * ib, hs, sizeof(float) * ib);
+        }
+        free(a_dq); free(h_dq); free(h); free(hq); free(hs);
+    }
+}
+
+/* The same expert FFN with every operand in FP32 and no quantisation (the all-FP32 layer):
+ * g, u, y are double-accumulated dot products rounded to FP32; h = silu(g)*u rounded to FP32.
+ * x [n_rows, H]; W13 [nE, 2I, H]; W2 [nE, H, I]; h_out [n_rows, I] may be NULL;
+ * y_out [n_rows, H] FP32. */
+void orc_ffn_f32(int64_t n_rows, int H, int I, const float* x, const int32_t* row_expert,
+                 const float* W13, const float* W2, float* h_out, float* y_out)
+{
+#pragma omp parallel
+    {
+        float* h = (float*)malloc(sizeof(float) * I);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int64_t e = row_expert[r];
+            const float* w13 = W13 + e * (int64_t)(2 * I) * H;
+            const float* w2 = W2 + e * (int64_t)H * I;
+            const float* xr = x + r * H;
+            for (int j = 0; j < I; ++j) {
+                double g = 0.0, u = 0.0;
+                for (int k = 0; k < H; ++k) {
+                    g += (double)xr[k] * (double)w13[(int64_t)j * H + k];
+                    u += (double)xr[k] * (double)w13[(int64_t)(I + j) * H + k];
+                }
+                h[j] = (float)(silu((double)(float)g) * (double)(float)u);
+            }
+            for (int n = 0; n < H; ++n) {
+                double y = 0.0;
+                for (int k = 0; k < I; ++k) y += (double)h[k] * (double)w2[(int64_t)n * I + k];
+                y_out[r * H + n] = (float)y;
+            }
+            if (h_out) memcpy(h_out + r * I, h, sizeof(float) * I);
+        }
+        free(h);
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1 §2.3] combine; [P2 §3.1] BF16 combine payload                                     */
+/* ------------------------------------------------------------------------------------ */
+
+/* y[t] = sum_k w[t,k] * yk[t,k] (FP32, slot order) + ysh[t] (if given), one FP32 result per
+ * element: each step is a separate FP32 multiply and FP32 add.  yk [n_tok, K, H] and ysh
+ * [n_tok, H] are FP32 or BF16 (y_is_bf16); acc_out [n_tok, H] FP32. */
+void orc_combine(int64_t n_tok, int K, int H, const void* yk, const void* ysh, int y_is_bf16,
+                 const float* w, float* acc_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n_tok; ++t) {
+        for (int n = 0; n < H; ++n) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                float prod = w[t * K + k] * load_elem(yk, y_is_bf16, (t * K + k) * H + n);
+                acc = acc + prod;
+            }
+            if (ysh) acc = acc + load_elem(ysh, y_is_bf16, t * H + n);
+            acc_out[t * H + n] = acc;
+        }
+    }
+}
