@@ -1,0 +1,419 @@
+"""Benchmark of the MoE layer forward (gate -> quantise -> permute -> grouped FP8 GEMM with
+SwiGLU -> grouped FP8 GEMM down-projection -> combine with the shared expert) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3_prefill] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one whole layer forward over T tokens of the named
+workload (default: the DeepSeek-V3-shaped prefill layer, T=16384).  Inputs are seeded
+synthetic tensors with the workload's shapes and distributions, resident in HBM before
+timing; the 11.3 GB of FP8 expert weights are far larger than L2, so no flush is needed.
+With N > 1 (torchrun), every rank runs its own T tokens (independent replicas, weak
+scaling; the layer has no cross-token exchange) and the slowest rank's time counts.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_gemm_sigmoid_b300 import moe, synthetic as sy  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+# kernels each entry point launches (memsets excluded); summed into gpu_launches
+LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_permute": 4,
+            "moe_grouped_gemm_fp8/swiglu": 3, "moe_grouped_gemm_fp8/store": 2,
+            "moe_combine": 1, "moe_bias_update": 1}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--config", default="v3_prefill", choices=sorted(sy.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle's timed sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            P = json.load(f)
+        return dict(hbm=P["hbm_gbs"], bf16=P["bf16_tflops"], bf16_sus=P["bf16_tflops_sustained"],
+                    src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+class Layer:
+    """Device-resident inputs, FP8 weights, outputs, staged intermediates and workspace."""
+
+    def __init__(self, cfg, dev):
+        self.cfg = cfg
+        T, H, I, E, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["n_experts"], cfg["top_k"]
+        S = int(cfg["has_shared"])
+        self.inp = sy.make_inputs(cfg, dev)
+        self.q = moe.quantize_weights(self.inp["W13"], self.inp["W2"])
+        self.x = self.inp["x"].view(torch.uint16)
+        self.weights = dict(Wg=self.inp["Wg"].view(torch.uint16), **self.q)
+        self.bias = self.inp["bias"].clone()
+        self.out = moe.empty_outputs(cfg, T, dev)
+        self.y = self.out["y"].view(torch.uint16)
+        self.ws = moe.workspace(cfg, T, dev)
+        R = T * K + T * S
+        self.R = R
+        u8, f32, i32 = torch.uint8, torch.float32, torch.int32
+        self.xq = torch.empty(T, H, dtype=u8, device=dev)
+        self.xs = torch.empty(T, H // 128, dtype=f32, device=dev)
+        self.offs = torch.empty(E + 2, dtype=i32, device=dev)
+        self.perm_tok = torch.empty(R, dtype=i32, device=dev)
+        self.row_of = torch.empty(T, K, dtype=i32, device=dev)
+        self.aq = torch.empty(R, H, dtype=u8, device=dev)
+        self.as_ = torch.empty(R, H // 128, dtype=f32, device=dev)
+        self.hq = torch.empty(R, I, dtype=u8, device=dev)
+        self.hs = torch.empty(R, I // 128, dtype=f32, device=dev)
+        self.yexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+
+    def forward(self):
+        o = self.out
+        moe.moe_forward(self.cfg, self.x, self.weights, self.bias, self.cfg["update_bias"], self.y,
+                        o["topk_idx"], o["topk_w"], o["counts"], self.ws)
+
+    STAGES = ["gate", "quant", "permute", "gemm1_swiglu", "gemm2_down", "combine", "bias_update"]
+
+    def staged(self, ev):
+        """The same layer through the individual entry points, an event after each stage."""
+        c, o = self.cfg, self.out
+        T, H, I, E = c["T"], c["hidden"], c["inter"], c["n_experts"]
+        G = E + int(c["has_shared"])
+        ev[0].record()
+        moe.moe_gate(c, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"])
+        ev[1].record()
+        moe.moe_quant_1x128(self.x, self.xq, self.xs)
+        ev[2].record()
+        moe.moe_permute(c, T, o["topk_idx"], o["counts"], self.xq, self.xs, self.offs, self.perm_tok,
+                        self.row_of, self.aq, self.as_, self.ws)
+        ev[3].record()
+        moe.moe_grouped_gemm_fp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
+                                 self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs, self.ws)
+        ev[4].record()
+        moe.moe_grouped_gemm_fp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
+                                 self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None, self.ws)
+        ev[5].record()
+        moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], self.y)
+        ev[6].record()
+        if c["update_bias"]:
+            moe.moe_bias_update(c, T, o["counts"], self.bias)
+        ev[7].record()
+
+    def launches_per_step(self):
+        n = sum(LAUNCHES[k] for k in ("moe_gate", "moe_quant_1x128", "moe_permute",
+                                      "moe_grouped_gemm_fp8/swiglu", "moe_grouped_gemm_fp8/store",
+                                      "moe_combine"))
+        return n + (LAUNCHES["moe_bias_update"] if self.cfg["update_bias"] else 0)
+
+
+def stage_work(cfg):
+    """Algorithmic work of each stage: FLOPs for the GEMMs, bytes for the rest."""
+    T, H, I, E, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["n_experts"], cfg["top_k"]
+    S = int(cfg["has_shared"])
+    R = T * K + T * S
+    return {
+        "gate": ("hbm", T * H * 2 + E * H * 2 + T * K * 8 + E * 4),
+        "quant": ("hbm", T * H * 2 + T * H + T * (H // 128) * 4),
+        "permute": ("hbm", T * K * 4 * 3 + R * (H + H // 128 * 4) + T * (H + H // 128 * 4)),
+        "gemm1_swiglu": ("tensor", 2 * R * H * 2 * I),
+        "gemm2_down": ("tensor", 2 * R * I * H),
+        "combine": ("hbm", R * H * 2 + T * H * 2 + T * K * 8),
+        "bias_update": ("hbm", E * 12),
+    }
+
+
+def barrier_sync(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(v, dist_on):
+    if not dist_on:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(cfg, layer, n_tok):
+    """The oracle, as it stands, on a bounded sample: the first n_tok tokens as a layer of its
+    own (gate, permutation, expert FFNs, combine).  Weight quantisation is offline on both
+    sides, so it is done before timing, for the experts the sample touches."""
+    import numpy as np
+    import oracle
+
+    sub = dict(cfg, T=n_tok)
+    x = layer.inp["x"][:n_tok].view(torch.uint16).cpu().numpy()
+    Wg = layer.inp["Wg"].view(torch.uint16).cpu().numpy()
+    bias = layer.inp["bias"].cpu().numpy()
+    W13, W2 = layer.inp["W13"], layer.inp["W2"]
+
+    def qfn(ids, cache={}):
+        miss = [int(e) for e in ids if int(e) not in cache]
+        if miss:
+            idx = torch.tensor(miss, device=W13.device)
+            w13 = W13.index_select(0, idx).view(torch.uint16).cpu().numpy()
+            w2 = W2.index_select(0, idx).view(torch.uint16).cpu().numpy()
+            q = oracle.quantize_weights(w13, w2)
+            for j, e in enumerate(miss):
+                cache[e] = tuple(a[j:j + 1] for a in q)
+        return tuple(np.concatenate([cache[int(e)][i] for e in ids]) for i in range(4))
+
+    g = oracle.gate(x, Wg, bias, cfg["n_group"], cfg["topk_group"], cfg["top_k"],
+                    cfg["routed_scaling_factor"])
+    ids = np.unique(np.concatenate([g["topk_idx"].ravel(), [cfg["n_experts"]]]))
+    qfn(ids)  # quantise outside the timed region
+    t0 = time.perf_counter()
+    oracle.forward(sub, x, Wg, bias, None, None, qweights=qfn)
+    dt = time.perf_counter() - t0
+    return dt, oracle.num_threads()
+
+
+def run_reference(args, cfg, rank, world):
+    """The reference arm: the CPU oracle timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    torch.cuda.set_device(0)
+    layer = Layer(cfg, "cuda:0")
+    n = max(1, min(args.cpu_sample // 4, cfg["T"]))
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, layer, n)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        dt, threads = cpu_baseline(cfg, layer, n)
+        times.append(dt)
+    tot = sum(times)
+    val = n * args.steps / tot
+    line = {
+        "impl": "reference", "metric": "MoE layer tokens/s (CPU oracle)", "value": val,
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "T": cfg["T"], "sample_tokens": n},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "first %d tokens of the %s batch as a layer of their own, per step" % (n, cfg["name"])},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = sy.config(args.config)
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank, world)
+    dist_on = world > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    peaks = load_peaks()
+    T = cfg["T"]
+    layer = Layer(cfg, dev)
+    stream = torch.cuda.current_stream()
+
+    # warm-up (W whole-layer steps through moe_forward and through the staged calls)
+    for _ in range(max(args.warmup, 3)):
+        layer.forward()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    for _ in range(2):
+        layer.staged(ev)
+    barrier_sync(dist_on)
+
+    # timed region 1: K steps of moe_forward (the headline)
+    clocks = Clocks(local)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier_sync(dist_on)
+    start.record(stream)
+    for _ in range(args.steps):
+        layer.forward()
+    stop.record(stream)
+    barrier_sync(dist_on)
+    clk = clocks.stop()
+    ms = max_over_ranks(start.elapsed_time(stop), dist_on)
+    assert moe.moe_device_error() == 0
+
+    # timed region 2: the same K steps through the staged entry points, per-stage events
+    stage_ms = {s: 0.0 for s in Layer.STAGES}
+    barrier_sync(dist_on)
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+        layer.staged(evs)
+        evs[-1].synchronize()
+        for i, s in enumerate(Layer.STAGES):
+            stage_ms[s] += evs[i].elapsed_time(evs[i + 1]) / args.steps
+    barrier_sync(dist_on)
+
+    # end to end: pinned host x -> device, moe_forward, y / routing / counts back to host
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty_like(layer.x, device="cpu").pin_memory()
+        x_host.copy_(layer.x)
+        o = layer.out
+        y_host = torch.empty_like(layer.y, device="cpu").pin_memory()
+        idx_host = torch.empty_like(o["topk_idx"], device="cpu").pin_memory()
+        w_host = torch.empty_like(o["topk_w"], device="cpu").pin_memory()
+        c_host = torch.empty_like(o["counts"], device="cpu").pin_memory()
+        x_dev = torch.empty_like(layer.x)
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_forward(cfg, x_dev, layer.weights, layer.bias, cfg["update_bias"], layer.y,
+                            o["topk_idx"], o["topk_w"], o["counts"], layer.ws)
+            y_host.copy_(layer.y, non_blocking=True)
+            idx_host.copy_(o["topk_idx"], non_blocking=True)
+            w_host.copy_(o["topk_w"], non_blocking=True)
+            c_host.copy_(o["counts"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier_sync(dist_on)
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        t2.record(stream)
+        barrier_sync(dist_on)
+        e2e_ms = max_over_ranks(s2.elapsed_time(t2), dist_on)
+        h2d = x_host.numel() * x_host.element_size()
+        d2h = sum(t.numel() * t.element_size() for t in (y_host, idx_host, w_host, c_host))
+        e2e = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    work = stage_work(cfg)
+    fp8_peak = peaks["bf16_sus"] * FP8_PER_BF16
+    stages = {}
+    for s in Layer.STAGES:
+        if s == "bias_update" and not cfg["update_bias"]:
+            continue
+        kind, amount = work[s]
+        t = stage_ms[s] / 1e3
+        if kind == "tensor":
+            ach = amount / t / 1e12 if t > 0 else None
+            stages[s] = {"ms": stage_ms[s], "TFLOP/s": ach, "frac_fp8_peak": ach / fp8_peak if ach else None}
+        else:
+            ach = amount / t / 1e9 if t > 0 else None
+            stages[s] = {"ms": stage_ms[s], "GB/s": ach, "frac_hbm": ach / peaks["hbm"] if ach else None}
+    dom = max(stages, key=lambda s: stages[s]["ms"])
+    kind, amount = work[dom]
+    dom_t = stage_ms[dom] / 1e3
+    if kind == "tensor":
+        roof = {"kernel": dom, "bound": "tensor", "achieved": amount / dom_t / 1e12, "peak": fp8_peak,
+                "unit": "TFLOP/s", "peak_source": "%s bf16 sustained x %.0f (nominal FP8:BF16)" % (peaks["src"], FP8_PER_BF16)}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": amount / dom_t / 1e9, "peak": peaks["hbm"],
+                "unit": "GB/s", "peak_source": "%s copy bandwidth" % peaks["src"]}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    gemm_ms = stage_ms["gemm1_swiglu"] + stage_ms["gemm2_down"]
+    gemm_tflops = (work["gemm1_swiglu"][1] + work["gemm2_down"][1]) / (gemm_ms / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(args.cpu_sample, T)
+        dt, threads = cpu_baseline(cfg, layer, n)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "first %d of the %d tokens as a layer of their own (gate, permutation, "
+                         "expert FFNs, combine; weights quantised beforehand)" % (n, T)}
+
+    line = {
+        "metric": "MoE layer tokens/s and grouped-GEMM TFLOPS (% of FP8 peak) at T=%d, 1 B300" % T,
+        "value": world * T * args.steps / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8-e4m3 (FP32 accumulation), bf16 activations",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "T": T, "hidden": cfg["hidden"], "inter": cfg["inter"],
+                   "n_experts": cfg["n_experts"], "top_k": cfg["top_k"], "shared": cfg["has_shared"],
+                   "l2": "inputs larger than L2 (11.3 GB of FP8 expert weights per step)",
+                   "parallelism": "replicas x%d" % world},
+        "grouped_gemm": {"ms": gemm_ms, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
+        "stages": stages,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": layer.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

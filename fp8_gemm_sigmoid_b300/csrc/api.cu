@@ -1,0 +1,180 @@
+// api.cu -- configuration checks, workspace layout, the grouped-GEMM dispatch, the gate
+// entry point and moe_forward (the whole layer on one stream).
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "gemm.h"
+
+namespace moe {
+
+// Device error word written by bounded waits in the kernels (0 = none).
+__device__ int g_device_error = 0;
+
+bool config_ok(const moe_config* c) {
+    if (!c) return false;
+    if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->n_group <= 0 ||
+        c->topk_group <= 0 || c->top_k <= 0)
+        return false;
+    if (c->n_experts % c->n_group != 0 || c->n_experts / c->n_group < 2) return false;
+    if (c->n_group > 32 || c->topk_group > c->n_group) return false;
+    if (c->top_k > c->topk_group * (c->n_experts / c->n_group)) return false;
+    if (c->n_experts > 1024 || c->top_k > 32) return false;
+    if (c->has_shared != 0 && c->has_shared != 1) return false;
+    if (c->mode != MOE_FP32 && c->mode != MOE_FP8_BLOCK) return false;
+    if (c->hidden % 128 != 0 || c->inter % 128 != 0) return false;
+    return true;
+}
+
+static size_t align_up(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
+
+WsLayout ws_layout(const moe_config& c, int64_t T) {
+    WsLayout L{};
+    const int64_t H = c.hidden, I = c.inter, E = c.n_experts, K = c.top_k, S = c.has_shared;
+    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const int64_t R = T * K + T * S;
+    L.R = R;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+    L.xq = take(fp8 ? T * H : 0);
+    L.xs = take(fp8 ? T * (H / 128) * 4 : 0);
+    L.offs = take((E + 2) * 4);
+    L.perm_tok = take(R * 4);
+    L.row_of = take(T * K * 4);
+    L.aq = take(fp8 ? R * H : R * H * 4);
+    L.as = take(fp8 ? R * (H / 128) * 4 : 0);
+    L.hq = take(fp8 ? R * I : R * I * 4);
+    L.hs = take(fp8 ? R * (I / 128) * 4 : 0);
+    L.yexp = take(fp8 ? R * H * 2 : R * H * 4);
+    L.perm_scratch = take(permute_scratch_bytes(T, static_cast<int>(E)));
+    L.gemm_scratch = take(gemm_scratch_bytes(static_cast<int32_t>(E + S), R, static_cast<int32_t>(2 * I),
+                                              MOE_EPI_SWIGLU_QUANT));
+    L.total = o;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration not supported";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA launch or runtime error";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait expired";
+    }
+    return "unknown moe_status";
+}
+
+extern "C" moe_status moe_config_validate(const moe_config* cfg) {
+    return config_ok(cfg) ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+extern "C" moe_status moe_workspace_size(const moe_config* cfg, int64_t T, size_t* bytes) {
+    if (!config_ok(cfg) || T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*cfg, T).total;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_device_error(int32_t* code) {
+    if (!code) return MOE_ERR_INVALID_ARG;
+    int v = 0;
+    MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
+    const int zero = 0;
+    MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
+    *code = v;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_gate(const moe_config* cfg, int64_t T, const void* x, const void* Wg,
+                               const float* bias, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, moe_stream_t stream) {
+    if (!config_ok(cfg) || T < 0 || !counts) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !Wg || !bias || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+    return launch_gate(*cfg, T, x, Wg, bias, topk_idx, topk_w, counts, nullptr,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                           int32_t N, int32_t Kdim, const uint8_t* A,
+                                           const float* As, const uint8_t* W, const float* Ws,
+                                           int32_t epilogue, void* out, float* out_s, void* ws,
+                                           size_t ws_bytes, moe_stream_t stream) {
+    if (n_groups < 1 || rows < 0 || N <= 0 || Kdim <= 0 || N % 128 || Kdim % 128)
+        return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_SWIGLU_QUANT) {
+        if (N % 256 != 0 || !out_s || !aligned16(out_s)) return MOE_ERR_INVALID_ARG;
+    } else if (epilogue != MOE_EPI_STORE) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    if (!offs || !A || !As || !W || !Ws || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(As) || !aligned16(W) || !aligned16(Ws) || !aligned16(out) ||
+        !aligned16(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < gemm_scratch_bytes(n_groups, rows, N, epilogue)) return MOE_ERR_WORKSPACE;
+    if (rows == 0) return MOE_OK;
+    return launch_grouped_gemm_fp8_simt(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue,
+                                        out, out_s, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* x,
+                                  const moe_weights* w, float* bias, int32_t update_bias,
+                                  void* y, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!config_ok(cfg) || T < 0 || !w || !counts || !ws || !bias) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = *cfg;
+    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    if (!w->Wg || !w->W13 || !w->W2 || (fp8 && (!w->W13_s || !w->W2_s))) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !y || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || (T > 0 && (!aligned16(x) || !aligned16(y)))) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c, T);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    const int64_t H = c.hidden, I = c.inter;
+    const int32_t G = c.n_experts + c.has_shared;
+    int32_t* offs = reinterpret_cast<int32_t*>(base + L.offs);
+    int32_t* perm_tok = reinterpret_cast<int32_t*>(base + L.perm_tok);
+    int32_t* row_of = reinterpret_cast<int32_t*>(base + L.row_of);
+    void* gscratch = base + L.gemm_scratch;
+    const size_t gbytes = L.total - L.gemm_scratch;
+
+    MOE_TRY(moe_gate(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, stream));
+    if (update_bias) MOE_TRY(moe_bias_update(cfg, T, counts, bias, stream));
+    if (T == 0) return MOE_OK;
+    if (fp8) {
+        uint8_t* xq = reinterpret_cast<uint8_t*>(base + L.xq);
+        float* xs = reinterpret_cast<float*>(base + L.xs);
+        uint8_t* aq = reinterpret_cast<uint8_t*>(base + L.aq);
+        float* as = reinterpret_cast<float*>(base + L.as);
+        uint8_t* hq = reinterpret_cast<uint8_t*>(base + L.hq);
+        float* hs = reinterpret_cast<float*>(base + L.hs);
+        void* yexp = base + L.yexp;
+        MOE_TRY(moe_quant_1x128(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
+        MOE_TRY(moe_permute(cfg, T, topk_idx, counts, xq, xs, offs, perm_tok, row_of, aq, as, ws,
+                            ws_bytes, stream));
+        MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, static_cast<int32_t>(2 * I), static_cast<int32_t>(H),
+                                     aq, as, static_cast<const uint8_t*>(w->W13), w->W13_s,
+                                     MOE_EPI_SWIGLU_QUANT, hq, hs, gscratch, gbytes, stream));
+        MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, static_cast<int32_t>(H), static_cast<int32_t>(I),
+                                     hq, hs, static_cast<const uint8_t*>(w->W2), w->W2_s,
+                                     MOE_EPI_STORE, yexp, nullptr, gscratch, gbytes, stream));
+        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, y, stream));
+    } else {
+        float* aq = reinterpret_cast<float*>(base + L.aq);
+        float* h = reinterpret_cast<float*>(base + L.hq);
+        float* yexp = reinterpret_cast<float*>(base + L.yexp);
+        MOE_TRY(moe_permute(cfg, T, topk_idx, counts, x, nullptr, offs, perm_tok, row_of, aq,
+                            nullptr, ws, ws_bytes, stream));
+        MOE_TRY(moe_grouped_gemm_f32(G, offs, L.R, static_cast<int32_t>(2 * I), static_cast<int32_t>(H),
+                                     aq, static_cast<const float*>(w->W13), MOE_EPI_SWIGLU_QUANT,
+                                     h, gscratch, gbytes, stream));
+        MOE_TRY(moe_grouped_gemm_f32(G, offs, L.R, static_cast<int32_t>(H), static_cast<int32_t>(I),
+                                     h, static_cast<const float*>(w->W2), MOE_EPI_STORE, yexp,
+                                     gscratch, gbytes, stream));
+        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, y, stream));
+    }
+    return MOE_OK;
+}

@@ -1,0 +1,65 @@
+// common.cuh -- device helpers shared by the libmoe kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+#define MOE_CUDA_CHECK(expr)                                                    \
+    do {                                                                        \
+        cudaError_t _e = (expr);                                                \
+        if (_e != cudaSuccess) return MOE_ERR_CUDA;                             \
+    } while (0)
+
+#define MOE_LAUNCH_CHECK()                                                      \
+    do {                                                                        \
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;             \
+    } while (0)
+
+#define MOE_TRY(expr)                                                           \
+    do {                                                                        \
+        moe_status _s = (expr);                                                 \
+        if (_s != MOE_OK) return _s;                                            \
+    } while (0)
+
+namespace moe {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// BF16 <-> FP32 (the BF16 bits are the upper half of the FP32 bits).
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Two FP32 -> two OCP E4M3 codes, round-to-nearest-even with saturation to +-448
+// (PTX cvt.rn.satfinite.e4m3x2.f32: the first source lands in the upper byte).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// OCP E4M3 code -> FP32 from the format's fields: bias 7, exponent field 0 = subnormal
+// m * 2^-9.  (Codes S.1111.111 are NaN; the quantiser never produces them.)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+    uint32_t s = (c & 0x80u) << 24, e = (c >> 3) & 15u, m = c & 7u;
+    float mag = (e == 0) ? static_cast<float>(m) * 0x1p-9f
+                         : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return __uint_as_float(__float_as_uint(mag) | s);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+}  // namespace moe

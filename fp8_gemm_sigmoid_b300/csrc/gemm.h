@@ -1,0 +1,30 @@
+// gemm.h -- grouped-GEMM launchers shared between translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Largest g with tile_start[g] <= tile (tile < tile_start[n_groups]).
+__device__ __forceinline__ int find_group(const int32_t* tile_start, int n_groups, int tile) {
+    int lo = 0, hi = n_groups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+moe_status launch_tile_prefix(int n_groups, int bm, const int32_t* offs, int32_t* tile_start,
+                              cudaStream_t s);
+moe_status launch_grouped_gemm_fp8_simt(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                        int32_t N, int32_t Kd, const uint8_t* A, const float* As,
+                                        const uint8_t* W, const float* Ws, int32_t epilogue,
+                                        void* out, float* out_s, void* ws, cudaStream_t s);
+__global__ void swiglu_quant_kernel(int I, const int32_t* offs_end, const float* gu,
+                                    uint8_t* hq, float* hs);
+
+}  // namespace moe

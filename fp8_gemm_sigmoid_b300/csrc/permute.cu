@@ -1,0 +1,161 @@
+// permute.cu -- a3: token permutation by expert (DeepSeek-V3 co-design teardown, §2.3:
+// per-expert counts, then the rows ordered by the argsort of the flat expert ids).
+//
+// The order is made deterministic and equal to a stable sort: rows are expert-major and,
+// within an expert, in ascending token order.  No atomics decide a position:
+//   1. chunk histogram: counts of each expert inside each chunk of kChunk tokens;
+//   2. scan: offs = exclusive prefix of the counts; base[c][e] = offs[e] + rows of expert e
+//      in chunks before c;
+//   3. positions: inside a chunk, one thread per expert walks the chunk's tokens in order;
+//   4. gather: each destination row copies its token's quantised row (and scales).
+// With a shared expert, group E follows with every token once, in order.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 64;  // tokens per chunk
+
+__global__ void __launch_bounds__(256)
+chunk_hist_kernel(int64_t T, int K, int E, const int32_t* __restrict__ idx,
+                  int32_t* __restrict__ chunk_cnt) {
+    extern __shared__ int32_t hist[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int64_t n = (T - t0 < kChunk ? T - t0 : kChunk) * K;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[idx[t0 * K + i]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One CTA; thread e (looping over experts) scans expert e's column over the chunks.
+__global__ void __launch_bounds__(1024)
+scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
+            const int32_t* __restrict__ counts, const int32_t* __restrict__ chunk_cnt,
+            int32_t* __restrict__ chunk_base, int32_t* __restrict__ offs) {
+    __shared__ int32_t part[1024];
+    // exclusive prefix over counts (E <= 1024): Hillis-Steele in shared memory
+    const int e = threadIdx.x;
+    int32_t v = (e < E) ? counts[e] : 0;
+    part[e] = v;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        int32_t add = (e >= o) ? part[e - o] : 0;
+        __syncthreads();
+        part[e] += add;
+        __syncthreads();
+    }
+    const int32_t incl = part[e];
+    if (e < E) {
+        const int32_t start = incl - v;
+        offs[e] = start;
+        int32_t run = start;
+#pragma unroll 8
+        for (int64_t c = 0; c < n_chunks; ++c) {
+            chunk_base[c * E + e] = run;
+            run += chunk_cnt[c * E + e];
+        }
+    }
+    if (e == 0) {
+        const int64_t routed = T * K;
+        offs[E] = static_cast<int32_t>(routed);
+        if (has_shared) offs[E + 1] = static_cast<int32_t>(routed + T);
+    }
+}
+
+// One CTA per chunk; thread e walks the chunk's tokens in order.
+__global__ void __launch_bounds__(256)
+positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restrict__ idx,
+                 const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_tok,
+                 int32_t* __restrict__ row_of) {
+    extern __shared__ int32_t sidx[];  // [kChunk * K]
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int nt = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
+    for (int i = threadIdx.x; i < nt * K; i += blockDim.x) sidx[i] = idx[t0 * K + i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t pos = chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+        for (int tt = 0; tt < nt; ++tt)
+            for (int k = 0; k < K; ++k)
+                if (sidx[tt * K + k] == e) {
+                    perm_tok[pos] = static_cast<int32_t>(t0 + tt);
+                    row_of[(t0 + tt) * K + k] = pos;
+                    ++pos;
+                }
+    }
+    if (has_shared)
+        for (int tt = threadIdx.x; tt < nt; tt += blockDim.x)
+            perm_tok[T * K + t0 + tt] = static_cast<int32_t>(t0 + tt);
+}
+
+// Copy row r of the destination from token perm_tok[r]: row_bytes payload (multiple of 16)
+// and, if scales, n_scales FP32 per row.
+__global__ void __launch_bounds__(128)
+gather_rows_kernel(int64_t R, int64_t row_bytes, int n_scales, const int32_t* __restrict__ perm_tok,
+                   const uint8_t* __restrict__ src, const float* __restrict__ src_s,
+                   uint8_t* __restrict__ dst, float* __restrict__ dst_s) {
+    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+        const int64_t t = perm_tok[r];
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + t * row_bytes);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + r * row_bytes);
+        for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) d4[i] = s4[i];
+        if (src_s)
+            for (int i = threadIdx.x; i < n_scales; i += blockDim.x)
+                dst_s[r * n_scales + i] = src_s[t * n_scales + i];
+    }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int64_t T, int E) {
+    const int64_t n_chunks = ceil_div(T > 0 ? T : 1, kChunk);
+    return static_cast<size_t>(2 * n_chunks * E) * sizeof(int32_t);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                                  const int32_t* counts, const void* xq, const float* xs,
+                                  int32_t* offs, int32_t* perm_tok, int32_t* row_of, void* aq,
+                                  float* as, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!config_ok(cfg) || T < 0) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = *cfg;
+    const int E = c.n_experts, K = c.top_k, S = c.has_shared;
+    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    if (!offs || !ws) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe::ws_layout(c, T).total) return MOE_ERR_WORKSPACE;
+    if (T > 0 && (!topk_idx || !counts || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;
+    if (fp8 && T > 0 && (!xs || !as || !aligned16(xs) || !aligned16(as))) return MOE_ERR_INVALID_ARG;
+    if ((T * K + T) >= 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t n_chunks = ceil_div(T, kChunk);
+    const moe::WsLayout L = moe::ws_layout(c, T);
+    int32_t* chunk_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.perm_scratch);
+    int32_t* chunk_base = chunk_cnt + n_chunks * E;
+    if (T == 0) {  // every group is empty
+        MOE_CUDA_CHECK(cudaMemsetAsync(offs, 0, sizeof(int32_t) * (E + 1 + S), s));
+        return MOE_OK;
+    }
+    chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
+        T, K, E, topk_idx, chunk_cnt);
+    MOE_LAUNCH_CHECK();
+    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, counts, chunk_cnt, chunk_base, offs);
+    MOE_LAUNCH_CHECK();
+    positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
+        T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
+    MOE_LAUNCH_CHECK();
+    const int64_t R = T * K + T * S;
+    const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
+    const int64_t grid = R < 148 * 64 ? R : 148 * 64;
+    gather_rows_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(
+        R, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
+        fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}

@@ -1,0 +1,220 @@
+/*
+ * moe.h -- C ABI of libmoe: the forward pass of a DeepSeek-V3-style fine-grained MoE layer
+ * on one B300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *  [P1] "从 1024 块 GPU 到 558 万美元：拆解 DeepSeek-V3 的算法-系统协同设计" (wsisp.com):
+ *       §2.2 MoEGate listing; §2.3 dispatch skeleton; §5.1 blockwise FP8 GEMM sketch.
+ *  [P2] "深入理解 DeepSeek-V3" (Chinese précis of "Insights into DeepSeek-V3: Scaling
+ *       Challenges and Reflections on Hardware for AI Architectures", arXiv 2505.09343):
+ *       §3.1 (8 routed + 1 shared expert, FP8 dispatch / BF16 combine);
+ *       §3.2 (1x128 activation tiles, 128x128 weight blocks, FP32 accumulation).
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers unless a parameter says "host".  The caller
+ *    allocates and owns every buffer (inputs, outputs, workspace); the library allocates
+ *    nothing, frees nothing and never synchronises the stream it is given.  Work is
+ *    enqueued on `stream` (NULL = the legacy default stream) and completes asynchronously.
+ *  - Row-major, densely packed tensors; shapes are given as [dim0, dim1, ...].
+ *    BF16 tensors are IEEE bfloat16 bit patterns (uint16); FP8 tensors are OCP E4M3 codes
+ *    (uint8); scales are FP32.
+ *  - A call returns MOE_OK after enqueueing its kernels, or an error code without
+ *    enqueueing anything when an argument is invalid.  MOE_ERR_CUDA reports a launch error
+ *    (cudaGetLastError).  No exception or longjmp crosses the ABI; no kernel traps.
+ *  - Calls on the same stream are ordered; calls that share a workspace must not overlap.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every entry point is exported from libmoe.so (the library is built with hidden default
+ * visibility). */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* a pointer is NULL or misaligned, or a size is out of range */
+    MOE_ERR_UNSUPPORTED = 2,  /* the configuration is valid but this build does not run it */
+    MOE_ERR_WORKSPACE = 3,    /* the workspace is smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+    MOE_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (see moe_device_error) */
+} moe_status;
+
+/* Numerics of the layer. */
+typedef enum moe_mode {
+    MOE_FP32 = 0,      /* x, gate weight, expert weights and y in FP32, no quantisation */
+    MOE_FP8_BLOCK = 1  /* x, gate weight and y in BF16; expert GEMMs on E4M3 operands with
+                          1x128 activation and 128x128 weight FP32 scales ([P2] §3.2) */
+} moe_mode;
+
+/* Layer configuration ([P1] §2.2: hidden_size, n_routed_experts, num_experts_per_tok,
+ * n_group, topk_group, routed_scaling_factor; [P1] §2.2 / [P2] §3.1: one shared expert).
+ * Valid when: hidden, inter, n_experts, n_group, topk_group, top_k > 0;
+ * n_experts % n_group == 0 and n_experts / n_group >= 2 (the group score sums two experts);
+ * topk_group <= n_group; top_k <= topk_group * n_experts / n_group; n_experts <= 1024;
+ * top_k <= 32; has_shared in {0, 1}; hidden % 128 == 0 and inter % 128 == 0 in both modes. */
+typedef struct moe_config {
+    int32_t hidden;      /* H: model width */
+    int32_t inter;       /* I: FFN width of each routed expert and of the shared expert */
+    int32_t n_experts;   /* E: routed experts */
+    int32_t n_group;     /* G: expert groups for group-limited routing */
+    int32_t topk_group;  /* TG: groups kept per token */
+    int32_t top_k;       /* K: routed experts per token */
+    float routed_scaling_factor; /* multiplies the (normalised) routing weights */
+    int32_t has_shared;  /* 1: add the always-on shared expert */
+    int32_t mode;        /* moe_mode */
+} moe_config;
+
+/* Epilogues of the grouped expert GEMM. */
+typedef enum moe_epilogue {
+    MOE_EPI_SWIGLU_QUANT = 0, /* W = stacked [gate; up] (N = 2I rows per group); output
+                                 h = silu(gate) * up quantised in 1x128 tiles (FP8 mode) or
+                                 h in FP32 (FP32 mode), [rows, I] */
+    MOE_EPI_STORE = 1         /* W = down projection (N = H rows per group); output [rows, N]
+                                 in BF16 (FP8 mode) or FP32 (FP32 mode) */
+} moe_epilogue;
+
+/* Expert weights of the layer.  Routed experts are slots 0..E-1 and the shared expert, if
+ * any, is slot E.
+ *  FP8 mode: W13 [E+S, 2I, H] E4M3 codes and W13_s [E+S, 2I/128, H/128] scales from
+ *            moe_quant_128x128 (rows 0..I-1 of each slot are the gate projection, rows
+ *            I..2I-1 the up projection); W2 [E+S, H, I] codes, W2_s [E+S, H/128, I/128].
+ *  FP32 mode: W13 [E+S, 2I, H] and W2 [E+S, H, I] FP32; the scale pointers are ignored.
+ *  Wg: gate weight [E, H], BF16 (FP8 mode) or FP32 (FP32 mode). */
+typedef struct moe_weights {
+    const void* Wg;
+    const void* W13;
+    const float* W13_s;
+    const void* W2;
+    const float* W2_s;
+} moe_weights;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* MOE_OK when *cfg satisfies the rules above, else MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_config_validate(const moe_config* cfg);
+
+/* Bytes of device workspace that moe_forward needs for T tokens (host out-param).  The
+ * same workspace also serves moe_permute and moe_grouped_gemm_* for that T. */
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, int64_t T, size_t* bytes);
+
+/* a1. [P1] §2.2 MoEGate, with the per-expert histogram of [P1] §2.3 fused in.
+ * logits = x . Wg^T accumulated in FP32; scores = sigmoid(logits); selection scores
+ * c = scores + bias (the bias steers selection only); group score = sum of the two largest
+ * c of each of the n_group groups; the topk_group best groups are kept and the other
+ * groups' experts are excluded; the top_k experts by c among the kept ones are chosen
+ * (ties to the lower index; slots in descending c); weights = scores (un-biased) at the
+ * chosen experts, divided by (their sum + 1e-20) if top_k > 1, times
+ * routed_scaling_factor.
+ *  x [T, H]: BF16 (FP8 mode) or FP32 (FP32 mode); Wg [E, H] same type; bias [E] FP32.
+ *  Outputs: topk_idx [T, K] int32, topk_w [T, K] FP32, counts [E] int32 (overwritten:
+ *  counts[e] = number of (token, slot) pairs routed to e).  T == 0 only zeroes counts. */
+MOE_API moe_status moe_gate(const moe_config* cfg, int64_t T, const void* x, const void* Wg,
+                    const float* bias, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                    moe_stream_t stream);
+
+/* a2. [P2] §3.2 activation quantisation in 1x128 tiles.  For every row and every 128
+ * consecutive columns: amax = max |x|; scale = amax / 448 and q = E4M3(x * (448 / amax))
+ * (round to nearest even, saturating to +-448); amax == 0 gives scale 1 and q = 0.
+ *  x [rows, cols] BF16, cols % 128 == 0; q [rows, cols] E4M3; s [rows, cols/128] FP32.
+ *  Pointers 16-byte aligned. */
+MOE_API moe_status moe_quant_1x128(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q,
+                           float* s, moe_stream_t stream);
+
+/* a2'. [P2] §3.2 weight quantisation in 128x128 blocks (same rule, one scale per block).
+ *  w [n_mats, rows, cols] BF16, rows % 128 == 0, cols % 128 == 0;
+ *  q [n_mats, rows, cols] E4M3; s [n_mats, rows/128, cols/128] FP32.  16-byte aligned. */
+MOE_API moe_status moe_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const uint16_t* w,
+                             uint8_t* q, float* s, moe_stream_t stream);
+
+/* a3. [P1] §2.3 token permutation by expert, deterministic: rows are expert-major and,
+ * within an expert, in ascending token order (the stable argsort of the flat expert ids).
+ * With has_shared, group E follows with every token once, in order.  R = T*K + T*S rows.
+ *  topk_idx [T, K] int32; counts [E] int32 (from moe_gate);
+ *  FP8 mode: xq [T, H] E4M3 and xs [T, H/128] FP32 (from moe_quant_1x128), gathered into
+ *            aq [R, H] and as [R, H/128];
+ *  FP32 mode: xq is x [T, H] FP32 gathered into aq [R, H] FP32; xs and as are ignored.
+ *  Outputs: offs [E + 1 + S] int32 (exclusive prefix sum of the rows per group),
+ *  perm_tok [R] int32 (token of each row), row_of [T, K] int32 (row of each (t, k)).
+ *  ws/ws_bytes: workspace of at least moe_workspace_size(cfg, T) bytes. */
+MOE_API moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                       const int32_t* counts, const void* xq, const float* xs, int32_t* offs,
+                       int32_t* perm_tok, int32_t* row_of, void* aq, float* as, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* a4/a5/a6. [P1] §5.1 / [P2] §3.2 grouped expert GEMM with blockwise FP8 operands and
+ * FP32 accumulation: for group g with rows [offs[g], offs[g+1]) and every output column n,
+ *   out[r, n] = sum_kb (as[r, kb] * Ws[g, n/128, kb]) * sum_{k in kb} A[r, k] * W[g, n, k]
+ * followed by the epilogue (moe_epilogue).  The shared expert is simply one more group.
+ *  n_groups >= 1; offs [n_groups + 1] device int32, non-decreasing, offs[0] == 0,
+ *  offs[n_groups] <= rows; rows = capacity (host) of A and out; N % 128 == 0 (for
+ *  SWIGLU_QUANT, N = 2I with I % 128 == 0); Kdim % 128 == 0.
+ *  A [rows, Kdim] E4M3, As [rows, Kdim/128]; W [n_groups, N, Kdim] E4M3,
+ *  Ws [n_groups, N/128, Kdim/128];
+ *  SWIGLU_QUANT: out [rows, N/2] E4M3 and out_s [rows, N/256] FP32 (the 1x128 quantisation
+ *  of h in FP32 -> FP8, no intermediate rounding); STORE: out [rows, N] BF16, out_s unused.
+ *  Rows beyond offs[n_groups] are left untouched.  16-byte aligned pointers. */
+MOE_API moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                int32_t N, int32_t Kdim, const uint8_t* A, const float* As,
+                                const uint8_t* W, const float* Ws, int32_t epilogue,
+                                void* out, float* out_s, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/* The same grouped GEMM with FP32 operands and no scales (FP32 mode):
+ *  A [rows, Kdim] FP32; W [n_groups, N, Kdim] FP32; SWIGLU_QUANT writes h [rows, N/2] FP32
+ *  (no quantisation); STORE writes out [rows, N] FP32. */
+MOE_API moe_status moe_grouped_gemm_f32(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                int32_t N, int32_t Kdim, const float* A, const float* W,
+                                int32_t epilogue, float* out, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/* a7. [P1] §2.3 (reverse exchange) / [P2] §3.1 (BF16 combine): for every token t,
+ *   y[t] = sum_{k=0..K-1} topk_w[t,k] * yexp[row_of[t,k]] + yexp[T*K + t]  (shared, if S)
+ * accumulated in FP32 in slot order, shared expert last, rounded once to the output type.
+ *  yexp [R, H] BF16 (FP8 mode) or FP32 (FP32 mode); row_of [T, K]; topk_w [T, K];
+ *  y [T, H] same type as yexp.  16-byte aligned. */
+MOE_API moe_status moe_combine(const moe_config* cfg, int64_t T, const void* yexp,
+                       const int32_t* row_of, const float* topk_w, void* y,
+                       moe_stream_t stream);
+
+/* a8. Load-driven selection-bias update (the bias "adjusted from real-time load" of
+ * [P1] §2.2): bias[i] += 1e-3 * sign(T*K/E - counts[i]), with the sign taken in integers
+ * (sign(T*K - E*counts[i])).  counts [E] int32, bias [E] FP32 updated in place. */
+MOE_API moe_status moe_bias_update(const moe_config* cfg, int64_t T, const int32_t* counts,
+                           float* bias, moe_stream_t stream);
+
+/* The whole layer forward on one stream: gate (a1), quantisation (a2, FP8 mode),
+ * permutation (a3), grouped GEMM with SwiGLU (a4), grouped GEMM down-projection (a5), with
+ * the shared expert as the last group (a6), combine (a7) and, if update_bias != 0, the bias
+ * update (a8) after routing.
+ *  x [T, H] BF16 (FP8) / FP32 (FP32); w: the weights; bias [E] FP32 (updated in place
+ *  when update_bias); outputs y [T, H] (type of x), topk_idx [T, K], topk_w [T, K],
+ *  counts [E] (the load histogram); ws/ws_bytes from moe_workspace_size(cfg, T). */
+MOE_API moe_status moe_forward(const moe_config* cfg, int64_t T, const void* x, const moe_weights* w,
+                       float* bias, int32_t update_bias, void* y, int32_t* topk_idx,
+                       float* topk_w, int32_t* counts, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Device-side error word written by bounded waits inside the kernels (0 = none).  Reading
+ * it synchronises the device.  *code receives the word; the call then clears it. */
+MOE_API moe_status moe_device_error(int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -257,17 +257,24 @@ def quantize_weights(W13, W2):
     return W13q, W13s, W2q, W2s
 
 
+def _take(W, ids):
+    """Rows `ids` of a stacked expert tensor: W[ids] for arrays, W(ids) for a callable that
+    returns them (lets a caller hand over only the experts a sample touches)."""
+    return np.ascontiguousarray(W(ids) if callable(W) else W[ids])
+
+
 def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     """The MoE layer forward: gate and permutation over all T tokens, then the expert FFNs
     and the combine for the tokens in `sample` (all tokens when None).  Every output row
     depends only on its own token, so a sample is exact.
 
     cfg: dict with hidden, inter, n_experts, n_group, topk_group, top_k,
-    routed_scaling_factor, has_shared, mode ('fp32' | 'fp8').  x [T,H] (f32 or BF16 bits),
-    W13 [E(+1),2I,H], W2 [E(+1),H,I]; the shared expert is the last slot.  In fp8 mode
-    `qweights` may carry quantize_weights(W13, W2) to skip re-quantising.
-    Returns dict with gate outputs, permutation, sample, y (BF16 bits in fp8 mode, f32 in
-    fp32 mode) and, in fp8 mode, the sampled xq/xs."""
+    routed_scaling_factor, has_shared, mode ('fp32' | 'fp8').  x [T,H] (f32 or BF16 bits);
+    W13 [E(+1),2I,H], W2 [E(+1),H,I] (the shared expert is the last slot), as arrays or as
+    callables ids -> stacked rows.  In fp8 mode `qweights(ids)` may return
+    quantize_weights(W13[ids], W2[ids]) from a cache.  Only the experts the sample touches
+    are read.  Returns dict with gate outputs, permutation, sample, y (BF16 bits in fp8
+    mode, f32 in fp32 mode), yexp [n, K(+1), H] and, in fp8 mode, the sampled xq/xs."""
     T = x.shape[0]
     E, K = cfg["n_experts"], cfg["top_k"]
     hs = int(bool(cfg["has_shared"]))
@@ -278,30 +285,32 @@ def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     sample = np.asarray(sample, dtype=np.int64)
     n = sample.size
     # one expert row per (sampled token, slot), then the shared expert row
-    row_tok = np.repeat(sample, K + hs)
     row_exp = np.empty((n, K + hs), np.int32)
     row_exp[:, :K] = g["topk_idx"][sample]
     if hs:
         row_exp[:, K] = E
     row_exp = row_exp.ravel()
+    needed, local = np.unique(row_exp, return_inverse=True)
+    local = local.astype(np.int32)
     out = dict(g, **p, sample=sample)
+    if n == 0:
+        out.update(y=np.empty((0, x.shape[1]), x.dtype), yexp=None)
+        return out
     if cfg["mode"] == "fp8":
-        xs_rows = np.ascontiguousarray(x[sample])
-        xq, xs = quant_1x128(xs_rows)
-        if qweights is None:
-            qweights = quantize_weights(W13, W2)
-        W13q, W13s, W2q, W2s = qweights
+        xq, xs = quant_1x128(np.ascontiguousarray(x[sample]))
+        if qweights is not None:
+            qw = qweights(needed)
+        else:
+            qw = quantize_weights(_take(W13, needed), _take(W2, needed))
         rep = np.repeat(np.arange(n), K + hs)
-        yrows = ffn_fp8(xq[rep], xs[rep], row_exp, W13q, W13s, W2q, W2s)
-        yrows = yrows.reshape(n, K + hs, -1)
+        yrows = ffn_fp8(xq[rep], xs[rep], local, *qw).reshape(n, K + hs, -1)
         acc = combine(yrows[:, :K], g["topk_w"][sample],
                       np.ascontiguousarray(yrows[:, K]) if hs else None)
         out.update(y=round_bf16(acc), yexp=yrows, xq=xq, xs=xs)
     else:
-        xr = np.ascontiguousarray(x[row_tok])
-        yrows = ffn_f32(xr, row_exp, W13, W2).reshape(n, K + hs, -1)
+        xr = np.ascontiguousarray(np.repeat(x[sample], K + hs, axis=0))
+        yrows = ffn_f32(xr, local, _take(W13, needed), _take(W2, needed)).reshape(n, K + hs, -1)
         acc = combine(yrows[:, :K], g["topk_w"][sample],
                       np.ascontiguousarray(yrows[:, K]) if hs else None)
         out.update(y=acc, yexp=yrows)
-    del row_tok
     return out

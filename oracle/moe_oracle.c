@@ -82,8 +82,24 @@ double orc_e4m3_to_double(uint8_t code)
     return s ? -v : v;
 }
 
-/* Magnitude of the non-negative finite code c (0..126), increasing in c. */
-static double e4m3_mag(int c) { return orc_e4m3_to_double((uint8_t)c); }
+/* Magnitudes of the non-negative finite codes 0..126 (increasing in the code), filled once
+ * from orc_e4m3_to_double. */
+static double g_mag[127];
+static int g_mag_ready = 0;
+
+static void mag_init(void)
+{
+    if (g_mag_ready) return;
+#pragma omp critical(orc_mag_init)
+    {
+        if (!g_mag_ready) {
+            for (int c = 0; c < 127; ++c) g_mag[c] = orc_e4m3_to_double((uint8_t)c);
+            g_mag_ready = 1;
+        }
+    }
+}
+
+static inline double e4m3_mag(int c) { return g_mag[c]; }
 
 /* FP32 -> E4M3 by the definition of round-to-nearest-even with saturation to the largest
  * finite value: pick the representable magnitude nearest to |v|; on an exact tie pick the
@@ -91,14 +107,15 @@ static double e4m3_mag(int c) { return orc_e4m3_to_double((uint8_t)c); }
  * NaN gives S.1111.111. */
 uint8_t orc_f32_to_e4m3(float v)
 {
+    mag_init();
     if (isnan(v)) return 0x7f;
     uint8_t sign = signbit(v) ? 0x80 : 0x00;
     double a = fabs((double)v);
     if (a >= 448.0) return sign | 0x7e;
-    int lo = 0, hi = 126; /* largest code whose magnitude is <= a */
-    while (lo < hi) {
-        int mid = (lo + hi + 1) / 2;
-        if (e4m3_mag(mid) <= a) lo = mid; else hi = mid - 1;
+    int lo = 0; /* largest code whose magnitude is <= a (binary search, fixed 7 steps) */
+    for (int step = 64; step > 0; step >>= 1) {
+        int m = lo + step;
+        lo = (m <= 126 && e4m3_mag(m) <= a) ? m : lo;
     }
     double dlo = a - e4m3_mag(lo), dhi = e4m3_mag(lo + 1) - a; /* both exact in double */
     int c;
@@ -219,6 +236,9 @@ void orc_gate(int64_t T, int H, int E, int G, int TG, int K, float rsf,
               int32_t* topk_idx, float* topk_w, float* scores_out, float* margin)
 {
     int gsz = E / G;
+    /* the gate weight widened to double once (exact) */
+    double* wd = (double*)malloc(sizeof(double) * (size_t)E * H);
+    for (int64_t i = 0; i < (int64_t)E * H; ++i) wd[i] = (double)load_elem(Wg, w_is_bf16, i);
 #pragma omp parallel
     {
         float* s = (float*)malloc(sizeof(float) * E);
@@ -226,14 +246,15 @@ void orc_gate(int64_t T, int H, int E, int G, int TG, int K, float rsf,
         float* gs = (float*)malloc(sizeof(float) * G);
         char* gkeep = (char*)malloc(G);
         char* taken = (char*)malloc(E);
+        double* xd = (double*)malloc(sizeof(double) * H);
 #pragma omp for schedule(dynamic, 16)
         for (int64_t t = 0; t < T; ++t) {
+            for (int h = 0; h < H; ++h) xd[h] = (double)load_elem(x, x_is_bf16, t * H + h);
             /* logits and sigmoid scores */
             for (int e = 0; e < E; ++e) {
+                const double* wr = wd + (int64_t)e * H;
                 double acc = 0.0;
-                for (int h = 0; h < H; ++h)
-                    acc += (double)load_elem(x, x_is_bf16, t * H + h) *
-                           (double)load_elem(Wg, w_is_bf16, (int64_t)e * H + h);
+                for (int h = 0; h < H; ++h) acc += xd[h] * wr[h];
                 float logit = (float)acc;
                 s[e] = (float)(1.0 / (1.0 + exp(-(double)logit)));
                 c[e] = s[e] + bias[e];
@@ -295,8 +316,9 @@ void orc_gate(int64_t T, int H, int E, int G, int TG, int K, float rsf,
             }
             for (int k = 0; k < K; ++k) topk_w[t * K + k] = w[k] * rsf;
         }
-        free(s); free(c); free(gs); free(gkeep); free(taken);
+        free(s); free(c); free(gs); free(gkeep); free(taken); free(xd);
     }
+    free(wd);
 }
 
 /* ------------------------------------------------------------------------------------ */

@@ -1,0 +1,86 @@
+"""The C-ABI library: it builds, loads and exports every entry point include/moe.h declares,
+and its host-side argument checks reject bad input without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from fp8_gemm_sigmoid_b300 import build, moe as m
+    build.build()
+    return m
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = header_symbols()
+    for n in ("moe_gate", "moe_quant_1x128", "moe_quant_128x128", "moe_permute",
+              "moe_grouped_gemm_fp8", "moe_combine", "moe_bias_update", "moe_forward",
+              "moe_workspace_size", "moe_status_string"):
+        assert n in names, n
+
+
+def test_library_exports_every_header_symbol(moe):
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in header_symbols():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(moe_\w+)", out))
+    assert set(header_symbols()) <= exported
+    assert set(moe.exported_symbols()) <= exported
+
+
+def test_config_validation(moe):
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    for name in sy.CONFIGS:
+        assert moe.moe_config_validate(sy.config(name))
+    base = sy.config("v3_prefill")
+    bad = [dict(base, n_group=7), dict(base, topk_group=9), dict(base, top_k=129),
+           dict(base, hidden=7000), dict(base, inter=100), dict(base, n_experts=8, n_group=8),
+           dict(base, has_shared=2), dict(base, top_k=0), dict(base, n_experts=2048, n_group=32)]
+    for c in bad:
+        assert not moe.moe_config_validate(c), c
+
+
+def test_workspace_size_grows_with_tokens(moe):
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    c = sy.config("v3_prefill")
+    a, b = moe.moe_workspace_size(c, 128), moe.moe_workspace_size(c, 16384)
+    assert 0 < a < b
+    # at least the permuted FP8 rows, their BF16 outputs and the FFN activations
+    R = 16384 * 9
+    assert b >= R * (7168 + 2 * 7168 + 2048)
+
+
+def test_host_side_argument_checks(moe):
+    L = moe._lib_handle()
+    vp = ctypes.c_void_p
+    # shapes that break the 1x128 / 128x128 contract are rejected before any launch
+    assert L.moe_quant_1x128(4, 100, vp(16), vp(16), vp(16), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quant_1x128(4, 128, None, vp(16), vp(16), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quant_1x128(4, 128, vp(17), vp(16), vp(16), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quant_128x128(1, 100, 128, vp(16), vp(16), vp(16), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_grouped_gemm_fp8(0, vp(16), 10, 256, 256, vp(16), vp(16), vp(16), vp(16), 0,
+                                  vp(16), vp(16), vp(16), 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_grouped_gemm_fp8(2, vp(16), 10, 256, 256, vp(16), vp(16), vp(16), vp(16), 7,
+                                  vp(16), vp(16), vp(16), 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_grouped_gemm_fp8(2, vp(16), 10, 256, 256, vp(16), vp(16), vp(16), vp(16), 0,
+                                  vp(16), vp(16), vp(16), 0, None) == moe.MOE_ERR_WORKSPACE
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    cfg = moe.make_config(sy.config("v3_prefill"))
+    need = ctypes.c_size_t(0)
+    assert L.moe_workspace_size(ctypes.byref(cfg), 1000, ctypes.byref(need)) == moe.MOE_OK
+    assert L.moe_permute(ctypes.byref(cfg), 1000, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16),
+                         vp(16), vp(16), vp(16), vp(16), need.value - 1, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_workspace_size(ctypes.byref(cfg), -1, ctypes.byref(need)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_status_string(moe.MOE_ERR_TIMEOUT).startswith(b"MOE_ERR_TIMEOUT")
