@@ -97,7 +97,7 @@ __device__ void select_token(const float* logit, int E, int G, int TG, int K, fl
         float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -INFINITY;
         int i = (lane < G && !((kept >> lane) & 1u)) ? lane : 0x7fffffff;
         warp_argmax(v, i);
-        kept |= 1u << i;
+        kept |= 1u << (i < G ? i : 0);  // a NaN score leaves no candidate: keep group 0
     }
     // top_k experts among the kept groups; experts of dropped groups are excluded
     uint32_t taken = 0;  // bit j: this lane's j-th expert already chosen
@@ -118,6 +118,7 @@ __device__ void select_token(const float* logit, int E, int G, int TG, int K, fl
         float bv = v;
         int bi = i;
         warp_argmax(bv, bi);
+        if (bi >= E) bi = 0;  // no candidate (NaN scores): fall back to expert 0, never out of range
         // the owner lane marks the expert and shares its un-biased score
         int owner = bi & 31;
         if (lane == owner) taken |= 1u << (bi >> 5);

@@ -103,20 +103,22 @@ grouped_gemm_fp8_simt_kernel(int n_groups, const int32_t* __restrict__ offs,
     for (int kb = 0; kb < kblocks; ++kb) {
         float p[4][4] = {};
         for (int k0 = kb * 128; k0 < kb * 128 + 128; k0 += kBK) {
-            // 64 rows x 32 codes per operand: thread tid loads 8 codes of A or of W
-            const int op = tid / 128, t2 = tid % 128, m = t2 / 4, c8 = (t2 % 4) * 8;
-            uint2 v;
+            // 64 rows x 32 codes per operand: thread tid loads 16 codes of A (tid < 128) or W
+            const int op = tid / 128, t2 = tid % 128, m = t2 / 2, c16 = (t2 % 2) * 16;
+            uint4 v;
             if (op == 0) {
                 const int64_t r = r0 + m;
-                v = (r < r_end) ? *reinterpret_cast<const uint2*>(A + r * Kd + k0 + c8) : make_uint2(0u, 0u);
+                v = (r < r_end) ? *reinterpret_cast<const uint4*>(A + r * Kd + k0 + c16)
+                                : make_uint4(0u, 0u, 0u, 0u);
             } else {
-                v = *reinterpret_cast<const uint2*>(Wg + static_cast<int64_t>(n0 + m) * Kd + k0 + c8);
+                v = *reinterpret_cast<const uint4*>(Wg + static_cast<int64_t>(n0 + m) * Kd + k0 + c16);
             }
             float (*dst)[kBM + 4] = (op == 0) ? As : Ws;
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[c8 + i][m] = e4m3_to_f32((v.x >> (8 * i)) & 0xffu);
+            for (int w4 = 0; w4 < 4; ++w4)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[c8 + 4 + i][m] = e4m3_to_f32((v.y >> (8 * i)) & 0xffu);
+                for (int i = 0; i < 4; ++i) dst[c16 + w4 * 4 + i][m] = e4m3_to_f32((vw[w4] >> (8 * i)) & 0xffu);
             __syncthreads();
 #pragma unroll 8
             for (int kk = 0; kk < kBK; ++kk) {

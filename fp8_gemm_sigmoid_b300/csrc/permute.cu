@@ -25,32 +25,39 @@ chunk_hist_kernel(int64_t T, int K, int E, const int32_t* __restrict__ idx,
     __syncthreads();
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     const int64_t n = (T - t0 < kChunk ? T - t0 : kChunk) * K;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[idx[t0 * K + i]], 1);
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t e = idx[t0 * K + i];
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);  // ids outside [0, E) are dropped
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         chunk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One CTA; thread e (looping over experts) scans expert e's column over the chunks.
+// One CTA.  Thread e totals expert e's column of chunk counts, an exclusive prefix over the
+// totals gives offs, and a second pass over the column gives each chunk's base.  The rows
+// are derived from topk_idx alone, so every position stays inside [0, T*K).
 __global__ void __launch_bounds__(1024)
 scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
-            const int32_t* __restrict__ counts, const int32_t* __restrict__ chunk_cnt,
-            int32_t* __restrict__ chunk_base, int32_t* __restrict__ offs) {
+            const int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base,
+            int32_t* __restrict__ offs) {
     __shared__ int32_t part[1024];
-    // exclusive prefix over counts (E <= 1024): Hillis-Steele in shared memory
     const int e = threadIdx.x;
-    int32_t v = (e < E) ? counts[e] : 0;
+    int32_t v = 0;
+    if (e < E) {
+#pragma unroll 8
+        for (int64_t c = 0; c < n_chunks; ++c) v += chunk_cnt[c * E + e];
+    }
     part[e] = v;
     __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) {
+    for (int o = 1; o < 1024; o <<= 1) {  // inclusive Hillis-Steele scan (E <= 1024)
         int32_t add = (e >= o) ? part[e - o] : 0;
         __syncthreads();
         part[e] += add;
         __syncthreads();
     }
-    const int32_t incl = part[e];
     if (e < E) {
-        const int32_t start = incl - v;
+        const int32_t start = part[e] - v;
         offs[e] = start;
         int32_t run = start;
 #pragma unroll 8
@@ -94,11 +101,13 @@ positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restr
 // Copy row r of the destination from token perm_tok[r]: row_bytes payload (multiple of 16)
 // and, if scales, n_scales FP32 per row.
 __global__ void __launch_bounds__(128)
-gather_rows_kernel(int64_t R, int64_t row_bytes, int n_scales, const int32_t* __restrict__ perm_tok,
-                   const uint8_t* __restrict__ src, const float* __restrict__ src_s,
-                   uint8_t* __restrict__ dst, float* __restrict__ dst_s) {
+gather_rows_kernel(int64_t R, int64_t T, int64_t row_bytes, int n_scales,
+                   const int32_t* __restrict__ perm_tok, const uint8_t* __restrict__ src,
+                   const float* __restrict__ src_s, uint8_t* __restrict__ dst,
+                   float* __restrict__ dst_s) {
     for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
         const int64_t t = perm_tok[r];
+        if (t < 0 || t >= T) continue;  // a row no valid (token, slot) claimed
         const uint4* s4 = reinterpret_cast<const uint4*>(src + t * row_bytes);
         uint4* d4 = reinterpret_cast<uint4*>(dst + r * row_bytes);
         for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) d4[i] = s4[i];
@@ -129,7 +138,8 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     const bool fp8 = (c.mode == MOE_FP8_BLOCK);
     if (!offs || !ws) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe::ws_layout(c, T).total) return MOE_ERR_WORKSPACE;
-    if (T > 0 && (!topk_idx || !counts || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
+    (void)counts;  // the rows are derived from topk_idx itself
     if (T > 0 && (!aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;
     if (fp8 && T > 0 && (!xs || !as || !aligned16(xs) || !aligned16(as))) return MOE_ERR_INVALID_ARG;
     if ((T * K + T) >= 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
@@ -145,7 +155,7 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
         T, K, E, topk_idx, chunk_cnt);
     MOE_LAUNCH_CHECK();
-    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, counts, chunk_cnt, chunk_base, offs);
+    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
     MOE_LAUNCH_CHECK();
     positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
         T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
@@ -154,7 +164,7 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
     const int64_t grid = R < 148 * 64 ? R : 148 * 64;
     gather_rows_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(
-        R, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
+        R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
         fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
     MOE_LAUNCH_CHECK();
     return MOE_OK;

@@ -144,7 +144,9 @@ MOE_API moe_status moe_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols,
 /* a3. [P1] §2.3 token permutation by expert, deterministic: rows are expert-major and,
  * within an expert, in ascending token order (the stable argsort of the flat expert ids).
  * With has_shared, group E follows with every token once, in order.  R = T*K + T*S rows.
- *  topk_idx [T, K] int32; counts [E] int32 (from moe_gate);
+ *  topk_idx [T, K] int32 with entries in [0, E) (as moe_gate writes them; an entry outside
+ *  that range is dropped and its row is left unwritten); counts [E]: the gate's histogram,
+ *  accepted for symmetry and not read (may be NULL) -- the rows are derived from topk_idx;
  *  FP8 mode: xq [T, H] E4M3 and xs [T, H/128] FP32 (from moe_quant_1x128), gathered into
  *            aq [R, H] and as [R, H/128];
  *  FP32 mode: xq is x [T, H] FP32 gathered into aq [R, H] FP32; xs and as are ignored.
