@@ -385,7 +385,7 @@ def main():
                          "expert FFNs, combine; weights quantised beforehand)" % (n, T)}
 
     line = {
-        "metric": "MoE layer tokens/s and grouped-GEMM TFLOPS (% of FP8 peak) at T=%d, 1 B300" % T,
+        "metric": "MoE layer tokens/s and grouped-GEMM TFLOPS (%% of FP8 peak) at T=%d, 1 B300" % T,
         "value": world * T * args.steps / (ms / 1e3),
         "unit": "tokens/s",
         "n_gpus": world,

@@ -221,7 +221,13 @@ def test_grouped_gemm_fp8_swiglu_and_down(moe, orc, H, I, E, R):
     assert np.allclose(to_host(hs), aux["hs"], rtol=1e-5, atol=0)
     step = np.repeat(aux["hs"], 128, axis=1) * 32.0  # largest E4M3 step (256..448) in code units
     assert np.all(np.abs(h_gpu - h_ref) <= step * 0.5 + 1e-30)
-    assert rel_err(h_gpu, h_ref) <= TOL_FP8
+    # the codes themselves agree except where h sits on a rounding boundary (FP32 sums in
+    # another order): at most one code step apart, and rarely
+    gq, rq_h = to_host(hq), aux["hq"]
+    diff = gq != rq_h
+    assert diff.mean() < 1e-3, diff.mean()
+    mag = lambda c: (c & 0x7F).astype(np.int32)  # noqa: E731  (codes ordered by magnitude)
+    assert np.all(np.abs(mag(gq[diff]) - mag(rq_h[diff])) <= 1)
     # GEMM2 on the GPU's own h, against the oracle's layer path
     assert rel_err(bf16_bits_to_f32(to_host(y)), bf16_bits_to_f32(yref)) <= TOL_FP8
 
