@@ -9,6 +9,8 @@
 //   3. positions: inside a chunk, one thread per expert walks the chunk's tokens in order;
 //   4. gather: each destination row copies its token's quantised row (and scales).
 // With a shared expert, group E follows with every token once, in order.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -152,6 +154,82 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
         MOE_CUDA_CHECK(cudaMemsetAsync(offs, 0, sizeof(int32_t) * (E + 1 + S), s));
         return MOE_OK;
     }
+    chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
+        T, K, E, topk_idx, chunk_cnt);
+    MOE_LAUNCH_CHECK();
+    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
+    MOE_LAUNCH_CHECK();
+    positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
+        T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
+    MOE_LAUNCH_CHECK();
+    const int64_t R = T * K + T * S;
+    const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
+    const int64_t grid = R < 148 * 64 ? R : 148 * 64;
+    gather_rows_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(
+        R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
+        fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// moe_permute_noalloc: the same permutation for callers that cannot hand over a workspace.
+// Its counters live in a fixed array in device memory that every GPU loading the library
+// holds until the process exits.  Every entry a call reads is written earlier in that same
+// call (chunk histogram, then bases), so nothing has to start at zero; two calls that run
+// on the GPU at the same time share the array and race.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = int64_t(1) << 20;  // 4 MiB: 2 * ceil(T/64) * E int32
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device, looked up once per device.
+// (In host code the symbol names a host-side shadow, not device memory.)
+moe_status noalloc_scratch(int32_t** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T,
+                                          const int32_t* topk_idx, const void* xq,
+                                          const float* xs, int32_t* offs, int32_t* perm_tok,
+                                          int32_t* row_of, void* aq, float* as,
+                                          moe_stream_t stream) {
+    if (!config_ok(cfg) || T < 0) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = *cfg;
+    const int E = c.n_experts, K = c.top_k, S = c.has_shared;
+    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    if (!offs) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;
+    if (fp8 && T > 0 && (!xs || !as || !aligned16(xs) || !aligned16(as))) return MOE_ERR_INVALID_ARG;
+    if ((T * K + T) >= 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+    const int64_t n_chunks = ceil_div(T, kChunk);
+    if (2 * n_chunks * E > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t* scratch = nullptr;
+    MOE_TRY(noalloc_scratch(&scratch));
+    if (T == 0) {
+        MOE_CUDA_CHECK(cudaMemsetAsync(offs, 0, sizeof(int32_t) * (E + 1 + S), s));
+        return MOE_OK;
+    }
+    int32_t* chunk_cnt = scratch;
+    int32_t* chunk_base = scratch + n_chunks * E;
     chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
         T, K, E, topk_idx, chunk_cnt);
     MOE_LAUNCH_CHECK();

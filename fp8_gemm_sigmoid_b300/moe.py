@@ -181,6 +181,17 @@ def moe_forward(cfg, x, weights, bias, update_bias, y, topk_idx, topk_w, counts,
         _stream(stream)))
 
 
+def moe_permute_noalloc(cfg, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as_, stream=None):
+    """moe_permute without a workspace: its counters live in libmoe's fixed device array
+    (see include/moe.h for the size limit and the rule that overlapping calls race)."""
+    f = _lib_handle().moe_permute_noalloc
+    f.argtypes = [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    f.restype = ctypes.c_int
+    _check("moe_permute_noalloc", f(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx), _ptr(xq), _ptr(xs),
+                                    _ptr(offs), _ptr(perm_tok), _ptr(row_of), _ptr(aq), _ptr(as_),
+                                    _stream(stream)))
+
+
 def moe_device_error():
     code = _i32(0)
     _check("moe_device_error", _lib_handle().moe_device_error(ctypes.byref(code)))

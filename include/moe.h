@@ -158,6 +158,28 @@ MOE_API moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_t* 
                        int32_t* perm_tok, int32_t* row_of, void* aq, float* as, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* moe_permute without a workspace (the pages have no counterpart; this is a library
+ * convenience).  For callers that cannot allocate device memory or hand over a workspace:
+ * code running inside a host framework that owns the whole device-memory budget and forbids
+ * extra allocations, latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation, and plugin interfaces whose signature carries only inputs and outputs.
+ * Same arguments, results and rules as moe_permute, minus counts, ws and ws_bytes.
+ *  - Scratch: a fixed 4 MiB array in device memory (file-scope, 256-byte aligned) that every
+ *    GPU which loads libmoe holds until the process exits.  Limit: 2 * ceil(T/64) * E <=
+ *    1,048,576 int32 (e.g. T <= 131072 at E = 256); larger calls return MOE_ERR_UNSUPPORTED
+ *    and enqueue nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call before any
+ *    stream capture.  MOE_ERR_CUDA if the lookup fails.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *  - Every call shares the array and overwrites it; nothing in it needs to start at zero.
+ *    Calls that overlap on the GPU (other streams, other threads) race and must be
+ *    serialised by the caller. */
+MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                               const void* xq, const float* xs, int32_t* offs,
+                               int32_t* perm_tok, int32_t* row_of, void* aq, float* as,
+                               moe_stream_t stream);
+
 /* a4/a5/a6. [P1] §5.1 / [P2] §3.2 grouped expert GEMM with blockwise FP8 operands and
  * FP32 accumulation: for group g with rows [offs[g], offs[g+1]) and every output column n,
  *   out[r, n] = sum_kb (as[r, kb] * Ws[g, n/128, kb]) * sum_{k in kb} A[r, k] * W[g, n, k]
