@@ -47,8 +47,9 @@ WsLayout ws_layout(const moe_config& c, int64_t T) {
     L.hs = take(fp8 ? R * (I / 128) * 4 : 0);
     L.yexp = take(fp8 ? R * H * 2 : R * H * 4);
     L.perm_scratch = take(permute_scratch_bytes(T, static_cast<int>(E)));
-    L.gemm_scratch = take(gemm_scratch_bytes(static_cast<int32_t>(E + S), R, static_cast<int32_t>(2 * I),
-                                              MOE_EPI_SWIGLU_QUANT));
+    L.gemm_scratch = take(fp8 ? tc_scratch_bytes(static_cast<int32_t>(E + S))
+                              : gemm_scratch_bytes(static_cast<int32_t>(E + S), R, static_cast<int32_t>(2 * I),
+                                                   MOE_EPI_SWIGLU_QUANT));
     L.total = o;
     return L;
 }
@@ -85,7 +86,9 @@ extern "C" moe_status moe_device_error(int32_t* code) {
     MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
     const int zero = 0;
     MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
-    *code = v;
+    int32_t tc = 0;
+    MOE_TRY(tc_read_and_clear_error(&tc));
+    *code = v ? v : tc;
     return MOE_OK;
 }
 
@@ -114,10 +117,10 @@ extern "C" moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs
     if (!aligned16(A) || !aligned16(As) || !aligned16(W) || !aligned16(Ws) || !aligned16(out) ||
         !aligned16(ws))
         return MOE_ERR_INVALID_ARG;
-    if (ws_bytes < gemm_scratch_bytes(n_groups, rows, N, epilogue)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < tc_scratch_bytes(n_groups)) return MOE_ERR_WORKSPACE;
     if (rows == 0) return MOE_OK;
-    return launch_grouped_gemm_fp8_simt(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue,
-                                        out, out_s, ws, reinterpret_cast<cudaStream_t>(stream));
+    return launch_grouped_gemm_fp8_tc(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue, out,
+                                      out_s, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* x,

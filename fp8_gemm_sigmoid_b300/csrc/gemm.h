@@ -24,6 +24,12 @@ moe_status launch_grouped_gemm_fp8_simt(int32_t n_groups, const int32_t* offs, i
                                         int32_t N, int32_t Kd, const uint8_t* A, const float* As,
                                         const uint8_t* W, const float* Ws, int32_t epilogue,
                                         void* out, float* out_s, void* ws, cudaStream_t s);
+moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N,
+                                      int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
+                                      const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
+                                      cudaStream_t s);
+size_t tc_scratch_bytes(int32_t n_groups);
+moe_status tc_read_and_clear_error(int32_t* code);
 __global__ void swiglu_quant_kernel(int I, const int32_t* offs_end, const float* gu,
                                     uint8_t* hq, float* hs);
 
