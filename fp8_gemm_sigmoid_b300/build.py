@@ -66,6 +66,7 @@ def build(force=False, verbose=False):
         raise RuntimeError("libmoe build failed")
     tmp = LIB + ".tmp%d" % os.getpid()
     link = [NVCC, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "shared",
+            "-Xlinker", "--no-undefined",
             *objs, "-o", tmp]
     subprocess.run(link, check=True)
     os.replace(tmp, LIB)

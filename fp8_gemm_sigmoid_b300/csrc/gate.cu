@@ -6,11 +6,20 @@
 // of the group, keep topk_group groups, top_k experts among them, weights from the
 // un-biased scores, normalised (top_k > 1) and scaled; §2.3: per-expert token counts.
 //
-// One CTA handles kTok tokens against all E experts: the [kTok, E] logit tile is formed in
-// shared memory (FP32 accumulation over H), then each warp runs the selection for its
-// tokens with warp shuffles (lane l holds experts l, l+32, ...).
+// Two kernels:
+//  - gate_tc_kernel (BF16 x and Wg, E <= 256): the [128 tokens x E] logit tile is one
+//    tcgen05 MMA accumulation in TMEM (BF16 x BF16 products are exact in FP32, FP32
+//    accumulation), fed by TMA; then one thread per token reads its logits back from TMEM
+//    and runs the selection in registers.  The kernel streams x once: HBM-bound.
+//  - gate_fused_kernel (FP32 inputs, or shapes outside the tensor-core kernel's range): the
+//    [kTok, E] logit tile is formed in shared memory on the CUDA cores, then each warp runs
+//    the selection for its tokens with warp shuffles (lane l holds experts l, l+32, ...).
+#include <mutex>
+
 #include "common.cuh"
+#include "gemm.h"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace moe {
 namespace {
@@ -199,6 +208,264 @@ gate_fused_kernel(int64_t Tn, int H, int E, int G, int TG, int K, float rsf,
     }
 }
 
+
+// ------------------------------------------------------------------------------------------
+// tensor-core gate
+// ------------------------------------------------------------------------------------------
+constexpr int kGtM = 128;           // tokens per CTA (MMA M)
+constexpr int kGtK = 64;            // BF16 columns per stage (128 bytes: one swizzle row)
+constexpr int kGtStages = 4;
+constexpr int kGtThreads = 256;     // warp 0 TMA, warp 1 MMA + TMEM, warps 4..7 selection
+constexpr int kGtMaxE = 256;
+constexpr int kGtMaxK = 8;
+constexpr int kGtMaxG = 8;
+constexpr int kGtABytes = kGtM * kGtK * 2;       // 16 KB
+constexpr int kGtBBytes = kGtMaxE * kGtK * 2;    // 32 KB (E rows)
+constexpr int kGtStageBytes = kGtABytes + kGtBBytes;
+constexpr int kGtSmem = kGtStages * kGtStageBytes + 4096;
+constexpr long long kGtWaitBudget = 4000000000LL;
+
+__device__ int g_gate_error = 0;
+
+struct GateTcParams {
+    int64_t T;
+    int H, E, G, TG, K;
+    float rsf;
+    const float* bias;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+};
+
+__global__ void __launch_bounds__(kGtThreads, 1)
+gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+               const GateTcParams p) {
+    using namespace sm100;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGtStages * kGtStageBytes);
+    uint64_t* empty = full + kGtStages;
+    uint64_t* acc_full = empty + kGtStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never = abort_flag + 1;
+    float* sbias = reinterpret_cast<float*>(tmem_slot + 4);        // [E]
+    int* shist = reinterpret_cast<int*>(sbias + kGtMaxE);           // [E]
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int nk = p.H / kGtK;
+    const uint32_t tmem_cols = 256;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGtStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        *never = 0;
+        fence_mbar_init();
+    }
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        sbias[e] = p.bias[e];
+        shist[e] = 0;
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kGtM;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmX);
+            tma_prefetch_desc(&tmW);
+            const uint32_t bytes = kGtABytes + p.E * kGtK * 2;
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            for (int kc = 0; kc < nk; ++kc) {
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kGtWaitBudget)) {
+                    *abort_flag = 1;
+                    atomicCAS(&g_gate_error, 0, 0x201);
+                    break;
+                }
+                uint8_t* sa = smem + s * kGtStageBytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                tma_load_2d(sa, &tmX, &full[s], kc * kGtK, static_cast<int32_t>(t0));
+                tma_load_2d(sa + kGtABytes, &tmW, &full[s], kc * kGtK, 0);
+                ++issued;
+                if (++s == kGtStages) { s = 0; ph ^= 1u; }
+            }
+            for (int i = 0; i < kGtStages && i < issued; ++i) {
+                if (--s < 0) { s = kGtStages - 1; ph ^= 1u; }
+                mbar_wait(&full[s], ph, never, kGtWaitBudget);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kGtM, p.E);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int kc = 0; kc < nk; ++kc) {
+                if (!mbar_wait(&full[s], ph, abort_flag, kGtWaitBudget)) {
+                    *abort_flag = 1;
+                    atomicCAS(&g_gate_error, 0, 0x202);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * kGtStageBytes);
+                const uint32_t b_addr = a_addr + kGtABytes;
+#pragma unroll
+                for (int k = 0; k < kGtK / 16; ++k)
+                    mma_bf16(tmem_base, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
+                             idesc, (kc > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&empty[s]);
+                if (++s == kGtStages) { s = 0; ph ^= 1u; }
+            }
+            mma_commit(acc_full);  // fires when every MMA above has completed
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------------- selection, one token per thread
+        const int quarter = warp & 3;
+        const int64_t t = t0 + quarter * 32 + lane;
+        const bool ok = mbar_wait(acc_full, 0, abort_flag, kGtWaitBudget);
+        tc_fence_after();
+        if (!ok) {
+            *abort_flag = 1;
+            atomicCAS(&g_gate_error, 0, 0x203);
+        } else {
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            const int gsz = p.E / p.G;   // a multiple of 32: each 32-column chunk lies in one group
+            const int cpg = gsz / 32;
+            float gs[kGtMaxG];
+            // pass 1: group scores = sum of the two largest selection scores of each group
+            for (int g = 0; g < kGtMaxG; ++g) {
+                float a1 = -INFINITY, a2 = -INFINITY;
+                if (g < p.G) {
+                    for (int cc = 0; cc < cpg; ++cc) {
+                        float l[32];
+                        tmem_ld32(taddr + (g * cpg + cc) * 32, l);
+                        tmem_ld_wait_regs(l);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float sv = 1.0f / (1.0f + expf(-l[j]));
+                            const float c = sv + sbias[(g * cpg + cc) * 32 + j];
+                            if (c > a1) { a2 = a1; a1 = c; } else if (c > a2) { a2 = c; }
+                        }
+                    }
+                }
+                gs[g] = a1 + a2;
+            }
+            // keep topk_group groups (ties to the lower index)
+            uint32_t kept = 0;
+            for (int r = 0; r < p.TG; ++r) {
+                int best = -1;
+                float bv = -INFINITY;
+#pragma unroll
+                for (int g = 0; g < kGtMaxG; ++g)
+                    if (g < p.G && !((kept >> g) & 1u) && (best < 0 || gs[g] > bv)) { best = g; bv = gs[g]; }
+                kept |= 1u << (best < 0 ? 0 : best);
+            }
+            // pass 2: top_k experts among the kept groups, in ascending expert order so that an
+            // equal score never displaces an earlier (lower-index) expert
+            float tv[kGtMaxK], ts[kGtMaxK];
+            int ti[kGtMaxK];
+#pragma unroll
+            for (int k = 0; k < kGtMaxK; ++k) { tv[k] = -INFINITY; ts[k] = 0.f; ti[k] = 0x7fffffff; }
+            // (every lane loads every chunk: tcgen05.ld is warp-collective; the group test only
+            // predicates the per-token processing)
+            for (int g = 0; g < p.G; ++g) {
+                const bool keep = (kept >> g) & 1u;
+                for (int cc = 0; cc < cpg; ++cc) {
+                    float l[32];
+                    tmem_ld32(taddr + (g * cpg + cc) * 32, l);
+                    tmem_ld_wait_regs(l);
+                    if (!keep) continue;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = (g * cpg + cc) * 32 + j;
+                        const float sv = 1.0f / (1.0f + expf(-l[j]));
+                        const float c = sv + sbias[e];
+                        // current K-th entry (compile-time indexing keeps the list in registers)
+                        float kv = -INFINITY;
+                        bool kfull = false;
+#pragma unroll
+                        for (int k = 0; k < kGtMaxK; ++k)
+                            if (k == p.K - 1) { kv = tv[k]; kfull = ti[k] != 0x7fffffff; }
+                        if (!kfull || c > kv) {
+                            // insert after every entry >= c
+                            float cv = c, cs = sv;
+                            int ci = e;
+#pragma unroll
+                            for (int k = 0; k < kGtMaxK; ++k) {
+                                if (k < p.K && (ti[k] == 0x7fffffff || cv > tv[k])) {
+                                    const float xv = tv[k], xs = ts[k];
+                                    const int xi = ti[k];
+                                    tv[k] = cv; ts[k] = cs; ti[k] = ci;
+                                    cv = xv; cs = xs; ci = xi;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            if (t < p.T) {
+                float den = 0.f;
+#pragma unroll
+                for (int k = 0; k < kGtMaxK; ++k)
+                    if (k < p.K) den = den + ts[k];
+                if (p.K > 1) den = den + 1e-20f;
+#pragma unroll
+                for (int k = 0; k < kGtMaxK; ++k) {
+                    if (k < p.K) {
+                        const int e = (ti[k] >= 0 && ti[k] < p.E) ? ti[k] : 0;
+                        const float w = (p.K > 1) ? ts[k] / den : ts[k];
+                        p.topk_idx[t * p.K + k] = e;
+                        p.topk_w[t * p.K + k] = w * p.rsf;
+                        atomicAdd(&shist[e], 1);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+        if (shist[e]) atomicAdd(&p.counts[e], shist[e]);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+bool gate_tc_supported(const moe_config& c) {
+    const int E = c.n_experts, G = c.n_group;
+    return c.mode == MOE_FP8_BLOCK && E % 32 == 0 && E <= kGtMaxE && G <= kGtMaxG &&
+           (E / G) % 32 == 0 && c.top_k <= kGtMaxK && c.hidden % kGtK == 0;
+}
+
+moe_status launch_gate_tc(const moe_config& c, int64_t T, const uint16_t* x, const uint16_t* Wg,
+                          const float* bias, int32_t* idx, float* w, int32_t* counts, cudaStream_t s) {
+    CUtensorMap tmX, tmW;
+    if (!make_tma_map_2d(&tmX, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, c.hidden, kGtM, kGtK))
+        return MOE_ERR_CUDA;
+    if (!make_tma_map_2d(&tmW, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.n_experts, c.hidden, c.n_experts, kGtK))
+        return MOE_ERR_CUDA;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
+    });
+    if (attr != cudaSuccess) return MOE_ERR_CUDA;
+    GateTcParams p{T, c.hidden, c.n_experts, c.n_group, c.topk_group, c.top_k, c.routed_scaling_factor,
+                   bias, idx, w, counts};
+    gate_tc_kernel<<<static_cast<unsigned>(ceil_div(T, kGtM)), kGtThreads, kGtSmem, s>>>(tmX, tmW, p);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
 }  // namespace
 
 size_t gate_scratch_bytes(const moe_config&, int64_t) { return 0; }
@@ -234,6 +501,9 @@ moe_status launch_gate(const moe_config& c, int64_t T, const void* x, const void
     if (c.mode == MOE_FP32)
         return launch_typed(c, T, static_cast<const float*>(x), static_cast<const float*>(Wg),
                             bias, idx, w, counts, s);
+    if (gate_tc_supported(c) && aligned16(x) && aligned16(Wg))
+        return launch_gate_tc(c, T, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
+                              bias, idx, w, counts, s);
     return launch_typed(c, T, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
                         bias, idx, w, counts, s);
 }

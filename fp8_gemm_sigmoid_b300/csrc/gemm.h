@@ -1,6 +1,7 @@
 // gemm.h -- grouped-GEMM launchers shared between translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,17 +21,16 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int n_group
 
 moe_status launch_tile_prefix(int n_groups, int bm, const int32_t* offs, int32_t* tile_start,
                               cudaStream_t s);
-moe_status launch_grouped_gemm_fp8_simt(int32_t n_groups, const int32_t* offs, int64_t rows,
-                                        int32_t N, int32_t Kd, const uint8_t* A, const float* As,
-                                        const uint8_t* W, const float* Ws, int32_t epilogue,
-                                        void* out, float* out_s, void* ws, cudaStream_t s);
 moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N,
                                       int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
                                       const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
                                       cudaStream_t s);
 size_t tc_scratch_bytes(int32_t n_groups);
 moe_status tc_read_and_clear_error(int32_t* code);
-__global__ void swiglu_quant_kernel(int I, const int32_t* offs_end, const float* gu,
-                                    uint8_t* hq, float* hs);
+// 2D TMA map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements, box
+// [box_rows x box_cols elements] (box_cols * elem_bytes == 128), 128-byte swizzle.
+bool make_tma_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                     int64_t rows, int64_t cols, int box_rows, int box_cols);
+int device_sm_count();
 
 }  // namespace moe

@@ -362,20 +362,22 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2D map over a row-major [rows, cols] byte matrix, box [128 rows x 128 bytes], 128B swizzle.
-bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+}  // namespace
+
+bool make_tma_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                     int64_t rows, int64_t cols, int box_rows, int box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    const cuuint32_t box[2] = {128, 128};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
+int device_sm_count() {
     static int n = 0;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -386,6 +388,10 @@ int sm_count() {
     return n > 0 ? n : 148;
 }
 
+namespace {
+bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+    return make_tma_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, 128, 128);
+}
 }  // namespace
 
 size_t tc_scratch_bytes(int32_t n_groups) {
@@ -425,7 +431,7 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t max_tiles = (ceil_div(rows, kBM) + n_groups) * p.n_tiles_n;
-    const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
+    const int grid = static_cast<int>(max_tiles < device_sm_count() ? max_tiles : device_sm_count());
     grouped_gemm_fp8_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
