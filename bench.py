@@ -38,13 +38,19 @@ LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_permute": 4,
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--config", default="v3_prefill", choices=sorted(sy.CONFIGS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle's timed sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    # smaller variants of the workload for profiler captures (same per-expert row count
+    # when T*top_k/experts is kept)
+    p.add_argument("--T", type=int, default=None)
+    p.add_argument("--experts", type=int, default=None)
+    p.add_argument("--groups", type=int, default=None)
+    p.add_argument("--topk-group", type=int, default=None)
     return p.parse_args()
 
 
@@ -69,7 +75,7 @@ class Clocks:
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
@@ -104,12 +110,15 @@ class Clocks:
 class Layer:
     """Device-resident inputs, FP8 weights, outputs, staged intermediates and workspace."""
 
-    def __init__(self, cfg, dev):
+    def __init__(self, cfg, dev, keep_bf16=True):
         self.cfg = cfg
         T, H, I, E, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["n_experts"], cfg["top_k"]
         S = int(cfg["has_shared"])
         self.inp = sy.make_inputs(cfg, dev)
         self.q = moe.quantize_weights(self.inp["W13"], self.inp["W2"])
+        if not keep_bf16:  # the BF16 expert weights only feed the CPU oracle
+            del self.inp["W13"], self.inp["W2"]
+            torch.cuda.empty_cache()
         self.x = self.inp["x"].view(torch.uint16)
         self.weights = dict(Wg=self.inp["Wg"].view(torch.uint16), **self.q)
         self.bias = self.inp["bias"].clone()
@@ -267,7 +276,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = sy.config(args.config)
+    over = {k: v for k, v in (("T", args.T), ("n_experts", args.experts), ("n_group", args.groups),
+                              ("topk_group", args.topk_group)) if v is not None}
+    cfg = sy.config(args.config, **over)
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
     dist_on = world > 1
@@ -277,7 +288,8 @@ def main():
     dev = "cuda:%d" % local
     peaks = load_peaks()
     T = cfg["T"]
-    layer = Layer(cfg, dev)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    layer = Layer(cfg, dev, keep_bf16=want_cpu)
     stream = torch.cuda.current_stream()
 
     # warm-up (W whole-layer steps through moe_forward and through the staged calls)
@@ -377,7 +389,7 @@ def main():
     gemm_tflops = (work["gemm1_swiglu"][1] + work["gemm2_down"][1]) / (gemm_ms / 1e3) / 1e12
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if want_cpu:
         n = min(args.cpu_sample, T)
         dt, threads = cpu_baseline(cfg, layer, n)
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
