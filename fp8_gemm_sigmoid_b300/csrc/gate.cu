@@ -275,6 +275,10 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kGtM;
+    // CTAs start their K sweep at different 64-column chunks so that concurrent loads of x
+    // (128 B from each of 128 rows) spread over the memory channels instead of all CTAs
+    // hitting the same column offsets at once.  The sum order is fixed per CTA.
+    const int kc0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * 37) % nk);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -284,7 +288,8 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
-            for (int kc = 0; kc < nk; ++kc) {
+            for (int it = 0; it < nk; ++it) {
+                const int kc = (it + kc0) % nk;
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kGtWaitBudget)) {
                     *abort_flag = 1;
                     atomicCAS(&g_gate_error, 0, 0x201);
@@ -307,7 +312,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const uint32_t idesc = idesc_bf16_f32(kGtM, p.E);
             int s = 0;
             uint32_t ph = 0;
-            for (int kc = 0; kc < nk; ++kc) {
+            for (int it = 0; it < nk; ++it) {
                 if (!mbar_wait(&full[s], ph, abort_flag, kGtWaitBudget)) {
                     *abort_flag = 1;
                     atomicCAS(&g_gate_error, 0, 0x202);
@@ -319,7 +324,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
                 for (int k = 0; k < kGtK / 16; ++k)
                     mma_bf16(tmem_base, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
-                             idesc, (kc > 0 || k > 0) ? 1u : 0u);
+                             idesc, (it > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&empty[s]);
                 if (++s == kGtStages) { s = 0; ph ^= 1u; }
             }

@@ -13,7 +13,7 @@
 //               per 128-wide K block into a 4-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates 512 TMEM columns; one lane issues 4 MMAs (K = 32 each) per K block
 //               into one of two 256-column FP32 partial buffers, then commits;
-//   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld), scale it by
+//   warps 2-9   promotion + epilogue: read the partial buffer (tcgen05.ld), scale it by
 //               as[r,kb] * Ws[g,nb,kb] into FP32 registers, release the buffer; after the last
 //               K block, either SwiGLU + 1x128 FP8 re-quantisation (gate/up GEMM) or BF16
 //               stores (down GEMM).
@@ -41,8 +41,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 promotion/epilogue
+constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -93,7 +93,7 @@ __device__ __forceinline__ int b_block(const TcParams& p, const TileCoord& c, in
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -139,7 +139,6 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int total = p.tile_start[p.n_groups];
 
     if (warp < kEpiWarp0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------------- producer
             int s = 0;
@@ -207,10 +206,10 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_wait(mma_done, 0, never, kWaitBudget);
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
         // -------------------------------------------------------------------- promotion + epilogue
+        // (10 warps per CTA and a 200-register cap leave room for the 128 FP32 accumulators)
         const int ew = warp - kEpiWarp0;       // 0..7
-        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
         const int set = ew / 4;                // column half within each 128-column half-tile
         const int trow = quarter * 32 + lane;  // row of the tile this thread owns
         const int col0 = set * 64, col1 = 128 + set * 64;
