@@ -13,7 +13,7 @@
 //               per 128-wide K block into a 4-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates 512 TMEM columns; one lane issues 4 MMAs (K = 32 each) per K block
 //               into one of two 256-column FP32 partial buffers, then commits;
-//   warps 2-9   promotion + epilogue: read the partial buffer (tcgen05.ld), scale it by
+//   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld), scale it by
 //               as[r,kb] * Ws[g,nb,kb] into FP32 registers, release the buffer; after the last
 //               K block, either SwiGLU + 1x128 FP8 re-quantisation (gate/up GEMM) or BF16
 //               stores (down GEMM).
@@ -41,8 +41,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 promotion/epilogue
-constexpr int kEpiWarp0 = 2;
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2-3 idle, warps 4..11 epilogue
+constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -93,7 +93,7 @@ __device__ __forceinline__ int b_block(const TcParams& p, const TileCoord& c, in
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -139,6 +139,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int total = p.tile_start[p.n_groups];
 
     if (warp < kEpiWarp0) {
+        // register split: 4 x 40 (TMA, MMA, 2 idle) + 8 x 232 (epilogue) = 12 x 168 per CTA
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------------- producer
             int s = 0;
@@ -206,8 +208,9 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_wait(mma_done, 0, never, kWaitBudget);
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
         // -------------------------------------------------------------------- promotion + epilogue
-        // (10 warps per CTA and a 200-register cap leave room for the 128 FP32 accumulators)
+        // 128 FP32 accumulators per thread plus one 16-column TMEM load in flight.
         const int ew = warp - kEpiWarp0;       // 0..7
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
         const int set = ew / 4;                // column half within each 128-column half-tile
@@ -239,22 +242,14 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(b * kBN);
-                float r0[32], r1[32];
-                tmem_ld32(taddr + col0, r0);
-                tmem_ld32(taddr + col0 + 32, r1);
-                tmem_ld_wait_regs(r0, r1);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    acc[i] = fmaf(r0[i], s0, acc[i]);
-                    acc[32 + i] = fmaf(r1[i], s0, acc[32 + i]);
-                }
-                tmem_ld32(taddr + col1, r0);
-                tmem_ld32(taddr + col1 + 32, r1);
-                tmem_ld_wait_regs(r0, r1);
+                for (int q = 0; q < 8; ++q) {
+                    float r[16];
+                    tmem_ld16(taddr + (q < 4 ? col0 + 16 * q : col1 + 16 * (q - 4)), r);
+                    tmem_ld_wait_regs16(r);
+                    const float sc = q < 4 ? s0 : s1;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    acc[64 + i] = fmaf(r0[i], s1, acc[64 + i]);
-                    acc[96 + i] = fmaf(r1[i], s1, acc[96 + i]);
+                    for (int i = 0; i < 16; ++i) acc[16 * q + i] = fmaf(r[i], sc, acc[16 * q + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
