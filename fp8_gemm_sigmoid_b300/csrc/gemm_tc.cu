@@ -178,12 +178,12 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             int s = 0;
             uint32_t ph = 0;
             int b = 0;
-            uint32_t pph[2] = {0u, 0u};
+            uint32_t pbits = 0;  // bit b: parity of the next use of partial buffer b
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, kWaitBudget)) { ok = false; break; }
-                    if (!mbar_wait(&pempty[b], pph[b] ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                    if (!mbar_wait(&pempty[b], ((pbits >> b) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
                     const uint32_t b_addr = a_addr + kABytes;
@@ -194,7 +194,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                    idesc, k > 0 ? 1u : 0u);
                     mma_commit(&empty[s]);
                     mma_commit(&pfull[b]);
-                    pph[b] ^= 1u;
+                    pbits ^= 1u << b;
                     b ^= 1;
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
@@ -217,8 +217,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int trow = quarter * 32 + lane;  // row of the tile this thread owns
         const int col0 = set * 64, col1 = 128 + set * 64;
         int b = 0;
-        uint32_t pph[2] = {0u, 0u};
-        uint32_t eph = 0;  // phase of ebar
+        uint32_t pbits = 0;  // bit b: parity of the next phase of pfull[b]
+        uint32_t eph = 0;    // phase of ebar
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TileCoord c = decode_tile(p, t);
@@ -234,11 +234,15 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.f;
             float sa_next = valid ? __ldg(as_row) : 0.f;
+            float w0_next = __ldg(ws0), w1_next = half1 ? __ldg(ws1) : 0.f;
             for (int kb = 0; kb < p.nkb; ++kb) {
-                const float sa = sa_next;
-                const float s0 = sa * __ldg(ws0 + kb), s1 = half1 ? sa * __ldg(ws1 + kb) : 0.f;
-                if (kb + 1 < p.nkb) sa_next = valid ? __ldg(as_row + kb + 1) : 0.f;
-                if (!mbar_wait(&pfull[b], pph[b], abort_flag, kWaitBudget)) { ok = false; break; }
+                const uint64_t s0 = splat2(sa_next * w0_next), s1 = splat2(sa_next * w1_next);
+                if (kb + 1 < p.nkb) {  // scales of the next block, loaded while this one runs
+                    sa_next = valid ? __ldg(as_row + kb + 1) : 0.f;
+                    w0_next = __ldg(ws0 + kb + 1);
+                    w1_next = half1 ? __ldg(ws1 + kb + 1) : 0.f;
+                }
+                if (!mbar_wait(&pfull[b], (pbits >> b) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(b * kBN);
@@ -247,14 +251,15 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     float r[16];
                     tmem_ld16(taddr + (q < 4 ? col0 + 16 * q : col1 + 16 * (q - 4)), r);
                     tmem_ld_wait_regs16(r);
-                    const float sc = q < 4 ? s0 : s1;
+                    const uint64_t sc = q < 4 ? s0 : s1;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * q + i] = fmaf(r[i], sc, acc[16 * q + i]);
+                    for (int i = 0; i < 16; i += 2)
+                        ffma2(acc[16 * q + i], acc[16 * q + i + 1], r[i], r[i + 1], sc);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pempty[b]);
-                pph[b] ^= 1u;
+                pbits ^= 1u << b;
                 b ^= 1;
             }
             if (!ok) break;

@@ -231,6 +231,23 @@ __device__ __forceinline__ void tmem_ld_wait_regs16(float (&r0)[16]) {
                  : "memory");
 }
 
+// Two FP32 fused multiply-adds in one instruction (PTX fma.rn.f32x2):
+// (a0, a1) = (b0, b1) * (s, s) + (a0, a1), each lane rounded as fmaf.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float b0, float b1, uint64_t s2) {
+    asm("{\n\t.reg .b64 a, b;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "fma.rn.f32x2 a, b, %4, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "l"(s2));
+}
+
+__device__ __forceinline__ uint64_t splat2(float s) {
+    const uint64_t u = __float_as_uint(s);
+    return u | (u << 32);
+}
+
 // Named barrier among `nthreads` threads (multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
