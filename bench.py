@@ -134,9 +134,9 @@ class Layer:
         self.perm_tok = torch.empty(R, dtype=i32, device=dev)
         self.row_of = torch.empty(T, K, dtype=i32, device=dev)
         self.aq = torch.empty(R, H, dtype=u8, device=dev)
-        self.as_ = torch.empty(R, H // 128, dtype=f32, device=dev)
+        self.as_ = torch.empty(H // 128, R, dtype=f32, device=dev)  # K-block-major
         self.hq = torch.empty(R, I, dtype=u8, device=dev)
-        self.hs = torch.empty(R, I // 128, dtype=f32, device=dev)
+        self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)  # K-block-major
         self.yexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
 
     def forward(self):

@@ -113,11 +113,10 @@ extern "C" moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs
     } else if (epilogue != MOE_EPI_STORE) {
         return MOE_ERR_INVALID_ARG;
     }
-    if (!offs || !A || !As || !W || !Ws || !out || !ws) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(As) || !aligned16(W) || !aligned16(Ws) || !aligned16(out) ||
-        !aligned16(ws))
+    if (!offs || !A || !As || !W || !Ws || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(As) || !aligned16(W) || !aligned16(Ws) || !aligned16(out))
         return MOE_ERR_INVALID_ARG;
-    if (ws_bytes < tc_scratch_bytes(n_groups)) return MOE_ERR_WORKSPACE;
+    (void)ws_bytes;  // the kernel builds its tile schedule in shared memory: no workspace
     if (rows == 0) return MOE_OK;
     return launch_grouped_gemm_fp8_tc(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue, out,
                                       out_s, ws, reinterpret_cast<cudaStream_t>(stream));

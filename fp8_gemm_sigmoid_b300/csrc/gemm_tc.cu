@@ -10,13 +10,19 @@
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles, warp-specialised:
 //   warp 0      TMA producer: A box [128 rows x 128 B] and two B boxes [128 rows x 128 B]
-//               per 128-wide K block into a 4-stage shared-memory ring (128-byte swizzle);
+//               per 128-wide K block into a 3-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates 512 TMEM columns; one lane issues 4 MMAs (K = 32 each) per K block
 //               into one of two 256-column FP32 partial buffers, then commits;
-//   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld), scale it by
-//               as[r,kb] * Ws[g,nb,kb] into FP32 registers, release the buffer; after the last
+//   warps 2-3   scale loaders: for each K block, the tile's 128 activation scales and its two
+//               weight scales go into a 4-slot shared-memory ring, so that the promotion warps
+//               issue no global loads (a pending global load stalls their tcgen05 fences);
+//   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld, 16 columns at a
+//               time with the next load in flight), scale it by as[kb,r] * Ws[g,nb,kb] into
+//               FP32 register pairs (packed FP32x2 FMA), release the buffer; after the last
 //               K block, either SwiGLU + 1x128 FP8 re-quantisation (gate/up GEMM) or BF16
-//               stores (down GEMM).
+//               output staged in shared memory and written by TMA stores (down GEMM).
+// Activation scales are K-block-major ([K/128, rows]) so that the 32 rows of a warp read one
+// contiguous 128-byte line per K block.
 // Because each K block lands in its own partial buffer, the per-block scaling is exact
 // (no FP22 accumulation, no scale folding) and overlaps the next block's MMAs.
 #include <cuda.h>
@@ -37,32 +43,43 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 256, kBK = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2-3 idle, warps 4..11 epilogue
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2-3 scales, warps 4..11 epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
-constexpr int kSmemBytes = kStages * kStageBytes + 4096;  // + alignment slack, barriers, amax exchange
+constexpr int kMaxGroups = 2048;
+constexpr int kOutBox = 32 * 128;                       // one warp's 32 rows x 128 B of output
+constexpr int kOutBytes = kEpiWarps * 2 * kOutBox;      // two staging boxes per epilogue warp
+constexpr int kScaleSlots = 4;
+constexpr int kSlotFloats = 136;  // 128 activation scales, 2 weight scales, padding to 16 bytes
+// Control block after the operand ring and the output staging (byte offsets): barriers,
+// TMEM address and flags, amax exchange, warp sums, scale ring, then the tile prefix.
+constexpr int kCtlBars = 0, kCtlSlot = 256, kCtlRed = 272, kCtlWarpSums = kCtlRed + 2048,
+              kCtlScales = kCtlWarpSums + 64, kCtlTiles = kCtlScales + kScaleSlots * kSlotFloats * 4;
+constexpr int kSmemFixed = 1024 + kStages * kStageBytes + kOutBytes + kCtlTiles;
+constexpr int kSmemMax = kSmemFixed + 4 * (kMaxGroups + 1);
 
-enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103 };
+enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103,
+             kErrTimeoutScales = 0x104 };
 
 struct TcParams {
     int n_groups;
     const int32_t* offs;        // [n_groups + 1]
-    const int32_t* tile_start;  // [n_groups + 1] tiles before group g
     int N;                      // rows of W per group
     int nkb;                    // K / 128
+    int rows;                   // row capacity of A, As and out
     int n_tiles_n;              // 256-column tiles per group
     int swiglu;                 // 1: gate/up pairing + FP8 re-quantisation; 0: BF16 store
-    const float* As;            // [rows, nkb]
+    const float* As;            // [nkb, rows] (K-block-major)
     const float* Ws;            // [n_groups, N/128, nkb]
     void* out;                  // SwiGLU: [rows, N/2] E4M3; store: [rows, N] BF16
-    float* out_s;               // SwiGLU: [rows, N/256]
+    float* out_s;               // SwiGLU: [N/256, rows] (K-block-major, as the next GEMM reads it)
 };
 
 struct TileCoord {
@@ -70,10 +87,10 @@ struct TileCoord {
     int row0, row_end;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(const TcParams& p, int t) {
+__device__ __forceinline__ TileCoord decode_tile(const TcParams& p, const int32_t* tile_start, int t) {
     TileCoord c;
-    c.g = find_group(p.tile_start, p.n_groups, t);
-    const int local = t - p.tile_start[c.g];
+    c.g = find_group(tile_start, p.n_groups, t);
+    const int local = t - tile_start[c.g];
     c.row0 = p.offs[c.g];
     c.row_end = p.offs[c.g + 1];
     const int mt = (c.row_end - c.row0 + kBM - 1) / kBM;
@@ -91,25 +108,97 @@ __device__ __forceinline__ int b_block(const TcParams& p, const TileCoord& c, in
     return 2 * c.n_tile + half;
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+// acc[base + i] += (r[2i], r[2i+1]) * (s, s) for i < 8: one packed FP32x2 FMA per column pair,
+// each lane rounded as a separate fmaf.
+__device__ __forceinline__ void scale_add16(float2 (&acc)[64], int base, const float (&r)[16], float2 s) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[base + i] = __ffma2_rn(make_float2(r[2 * i], r[2 * i + 1]), s, acc[base + i]);
+}
+
+// 2D TMA store of a [32 rows x 128 B] box from shared memory (128-byte swizzle) at (x, y).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Tiles of group g: ceil(rows_g / 128) m-tiles times the n-tiles of one group.
+__device__ __forceinline__ int group_tiles(const TcParams& p, int g) {
+    return ((p.offs[g + 1] - p.offs[g] + kBM - 1) / kBM) * p.n_tiles_n;
+}
+
+// tile_start[g] = tiles of the groups before g (g = 0..n_groups), computed by the whole CTA
+// from the device-side row offsets: each thread sums a run of consecutive groups, a block
+// scan of the run totals gives each run's start, and the thread writes its run's prefixes.
+__device__ void tile_prefix(const TcParams& p, int32_t* warp_sums, int32_t* tile_start) {
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    const int per = (p.n_groups + kThreads - 1) / kThreads;
+    const int g0 = min(tid * per, p.n_groups), g1 = min(g0 + per, p.n_groups);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += group_tiles(p, g);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kThreads / 32 ? warp_sums[lane] : 0;
+        const int own = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
+        }
+        if (lane < kThreads / 32) warp_sums[lane] = w - own;  // exclusive warp offsets
+    }
+    __syncthreads();
+    int run = warp_sums[warp] + incl - sum;
+    for (int g = g0; g < g1; ++g) {
+        tile_start[g] = run;
+        run += group_tiles(p, g);
+    }
+    if (g0 < g1 && g1 == p.n_groups) tile_start[p.n_groups] = run;
+    __syncthreads();
+}
+
+// silu(g) = g * sigmoid(g) with the fast exponential and division intrinsics: h is quantised
+// to E4M3 (3 mantissa bits) right after, so their few-ulp FP32 error only matters on a code
+// boundary, where the FP32 accumulation order already decides.  g -> -inf gives -0.
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmO, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint8_t* out_stage = smem + kStages * kStageBytes;   // [8 warps][2 halves][32 x 128 B]
+    uint8_t* ctl = out_stage + kOutBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ctl + kCtlBars);
     uint64_t* full = bars;                  // [kStages]  TMA -> MMA
     uint64_t* empty = bars + kStages;       // [kStages]  MMA -> TMA
     uint64_t* pfull = bars + 2 * kStages;   // [2]        MMA -> epilogue
     uint64_t* pempty = pfull + 2;           // [2]        epilogue -> MMA
     uint64_t* mma_done = pempty + 2;        // [1]        final MMA drain
     uint64_t* ebar = mma_done + 1;          // [1]        epilogue amax exchange (one phase per tile)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
+    uint64_t* sfull = ebar + 1;             // [kScaleSlots] scale loaders -> epilogue
+    uint64_t* sempty = sfull + kScaleSlots; // [kScaleSlots] epilogue -> scale loaders
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + kCtlSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;   // stays 0: drains wait for in-flight work, not for aborts
-    float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2 tiles][2 sets][128 rows] amax exchange
+    float* red = reinterpret_cast<float*>(ctl + kCtlRed);  // [2 tiles][2 sets][128 rows] amax exchange
+    int32_t* warp_sums = reinterpret_cast<int32_t*>(ctl + kCtlWarpSums);  // [kThreads / 32]
+    float* sring = reinterpret_cast<float*>(ctl + kCtlScales);         // [kScaleSlots][kSlotFloats]
+    int32_t* tile_start = reinterpret_cast<int32_t*>(ctl + kCtlTiles);  // [n_groups + 1]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -123,6 +212,10 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         mbar_init(mma_done, 1);
         mbar_init(ebar, kEpiThreads);
+        for (int i = 0; i < kScaleSlots; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], kEpiWarps);
+        }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -131,15 +224,16 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (!p.swiglu) tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
-    __syncthreads();
+    tile_prefix(p, warp_sums, tile_start);  // contains the CTA barriers that publish the set-up
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = p.tile_start[p.n_groups];
+    const int total = tile_start[p.n_groups];
 
     if (warp < kEpiWarp0) {
-        // register split: 4 x 40 (TMA, MMA, 2 idle) + 8 x 232 (epilogue) = 12 x 168 per CTA
+        // register split: 4 x 40 (TMA, MMA, 2 scale loaders) + 8 x 232 (epilogue) = 12 x 168
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------------- producer
@@ -148,7 +242,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             int issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileCoord c = decode_tile(p, t);
+                const TileCoord c = decode_tile(p, tile_start, t);
                 const int brow0 = c.g * p.N + b_block(p, c, 0) * 128;
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -206,59 +300,115 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             // drain: every MMA this thread issued has completed once mma_done flips
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, never, kWaitBudget);
+        } else if (warp == 2 || warp == 3) {
+            // ---------------------------------------------------------------- scale loaders
+            // Warp 2 fills the slots of the even K-block counts, warp 3 the odd ones; each warp
+            // loads its next block's scales into registers while it waits for the slot.
+            const int my_tiles = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+            const int kc_total = my_tiles * p.nkb;
+            float v[4], w0 = 0.f, w1 = 0.f;
+            auto fetch = [&](int kc) {
+                const TileCoord c = decode_tile(p, tile_start, blockIdx.x + (kc / p.nkb) * gridDim.x);
+                const int kb = kc % p.nkb;
+                const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = c.row0 + lane + 32 * j;
+                    v[j] = r < c.row_end ? __ldg(col + r) : 0.f;
+                }
+                const int64_t nbk = p.N / 128;
+                const int b1 = b_block(p, c, 1);
+                w0 = __ldg(p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb + kb);
+                w1 = b1 < nbk ? __ldg(p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb + kb) : 0.f;
+            };
+            uint32_t sph = 0;  // bit i: parity of the next use of slot i
+            bool ok = true;
+            int kc = warp & 1;
+            if (kc < kc_total) fetch(kc);
+            for (; kc < kc_total; kc += 2) {
+                const int i = kc % kScaleSlots;
+                if (!mbar_wait(&sempty[i], ((sph >> i) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                sph ^= 1u << i;
+                float* slot = sring + i * kSlotFloats;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) slot[lane + 32 * j] = v[j];
+                if (lane == 0) {
+                    slot[128] = w0;
+                    slot[129] = w1;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfull[i]);
+                if (kc + 2 < kc_total) fetch(kc + 2);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicCAS(&g_tc_error, 0, kErrTimeoutScales);
+            }
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
         // -------------------------------------------------------------------- promotion + epilogue
-        // 128 FP32 accumulators per thread plus one 16-column TMEM load in flight.
+        // 128 FP32 accumulators per thread (64 pairs) plus two 16-column TMEM staging chunks.
         const int ew = warp - kEpiWarp0;       // 0..7
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
         const int set = ew / 4;                // column half within each 128-column half-tile
         const int trow = quarter * 32 + lane;  // row of the tile this thread owns
         const int col0 = set * 64, col1 = 128 + set * 64;
+        uint8_t* my_stage = out_stage + ew * 2 * kOutBox;
         int b = 0;
         uint32_t pbits = 0;  // bit b: parity of the next phase of pfull[b]
         uint32_t eph = 0;    // phase of ebar
+        uint32_t sfp = 0;    // bit i: parity of the next phase of sfull[i]
+        int kc = 0;          // K blocks promoted so far (scale ring position)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileCoord c = decode_tile(p, t);
+            const TileCoord c = decode_tile(p, tile_start, t);
             const int row = c.row0 + trow;
             const bool valid = row < c.row_end;
-            const float* as_row = p.As + static_cast<int64_t>(valid ? row : c.row0) * p.nkb;
-            const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * (p.N / 128) + b_block(p, c, 0)) * p.nkb;
             // in the down GEMM the last tile's second half lies past N when N % 256 == 128: it is
             // computed from whatever rows follow (zeros past the tensor) and never stored
             const bool half1 = b_block(p, c, 1) < p.N / 128;
-            const float* ws1 = p.Ws + (static_cast<int64_t>(c.g) * (p.N / 128) + (half1 ? b_block(p, c, 1) : 0)) * p.nkb;
-            float acc[128];
+            float2 acc[64];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-            float sa_next = valid ? __ldg(as_row) : 0.f;
-            float w0_next = __ldg(ws0), w1_next = half1 ? __ldg(ws1) : 0.f;
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const uint64_t s0 = splat2(sa_next * w0_next), s1 = splat2(sa_next * w1_next);
-                if (kb + 1 < p.nkb) {  // scales of the next block, loaded while this one runs
-                    sa_next = valid ? __ldg(as_row + kb + 1) : 0.f;
-                    w0_next = __ldg(ws0 + kb + 1);
-                    w1_next = half1 ? __ldg(ws1 + kb + 1) : 0.f;
-                }
+            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
+            for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
+                // this block's scales from the ring: as[kb, row] * Ws[g, half, kb]
+                const int si = kc % kScaleSlots;
+                if (!mbar_wait(&sfull[si], (sfp >> si) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                sfp ^= 1u << si;
+                const float* slot = sring + si * kSlotFloats;
+                const float sa = slot[trow];
+                const float sc0 = sa * slot[128], sc1 = sa * slot[129];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[si]);
+                const float2 s0 = make_float2(sc0, sc0), s1 = make_float2(sc1, sc1);
                 if (!mbar_wait(&pfull[b], (pbits >> b) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(b * kBN);
+                // eight 16-column chunks (gate half at col0, up half at col1); the next chunk's
+                // TMEM load is in flight while the current chunk is scaled, and the buffer is
+                // released as soon as the last load has landed
+                float ra[16], rb[16];
+                tmem_ld16(taddr + col0, ra);
+                tmem_ld_wait_regs16(ra);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float r[16];
-                    tmem_ld16(taddr + (q < 4 ? col0 + 16 * q : col1 + 16 * (q - 4)), r);
-                    tmem_ld_wait_regs16(r);
-                    const uint64_t sc = q < 4 ? s0 : s1;
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2)
-                        ffma2(acc[16 * q + i], acc[16 * q + i + 1], r[i], r[i + 1], sc);
+                for (int q = 0; q < 7; ++q) {
+                    const int cn = (q + 1 < 4) ? col0 + 16 * (q + 1) : col1 + 16 * (q - 3);
+                    if (q % 2 == 0) {
+                        tmem_ld16(taddr + cn, rb);
+                        scale_add16(acc, 8 * q, ra, q < 4 ? s0 : s1);
+                        tmem_ld_wait_regs16(rb);
+                    } else {
+                        tmem_ld16(taddr + cn, ra);
+                        scale_add16(acc, 8 * q, rb, q < 4 ? s0 : s1);
+                        tmem_ld_wait_regs16(ra);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pempty[b]);
+                scale_add16(acc, 56, rb, s1);
                 pbits ^= 1u << b;
                 b ^= 1;
             }
@@ -269,9 +419,10 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int I = p.N / 2;
                 float amax = 0.f;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    acc[j] = silu_f32(acc[j]) * acc[64 + j];
-                    amax = fmaxf(amax, fabsf(acc[j]));
+                for (int j = 0; j < 32; ++j) {
+                    acc[j].x = silu_f32(acc[j].x) * acc[32 + j].x;
+                    acc[j].y = silu_f32(acc[j].y) * acc[32 + j].y;
+                    amax = fmaxf(amax, fmaxf(fabsf(acc[j].x), fabsf(acc[j].y)));
                 }
                 float* rb = red + eph * 256;  // double-buffered by tile
                 rb[set * 128 + trow] = amax;
@@ -288,8 +439,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const float mul = __fdiv_rn(448.f, amax);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(acc[4 * i], mul), __fmul_rn(acc[4 * i + 1], mul));
-                            const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(acc[4 * i + 2], mul), __fmul_rn(acc[4 * i + 3], mul));
+                            const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(acc[2 * i].x, mul), __fmul_rn(acc[2 * i].y, mul));
+                            const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(acc[2 * i + 1].x, mul), __fmul_rn(acc[2 * i + 1].y, mul));
                             pk[i] = lo | (hi << 16);
                         }
                     }
@@ -297,24 +448,46 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                           static_cast<int64_t>(row) * I + c.n_tile * 128 + set * 64);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                    if (set == 0) p.out_s[static_cast<int64_t>(row) * (I / 128) + c.n_tile] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+                    if (set == 0)
+                        p.out_s[static_cast<int64_t>(c.n_tile) * p.rows + row] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
                 }
-            } else if (valid) {
-                uint16_t* orow = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(row) * p.N + c.n_tile * kBN;
+            } else {
+                // BF16 output.  A warp whose 32 rows all belong to this group stages them in
+                // shared memory (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8))
+                // and one lane writes each 32 x 64 box with a TMA store; a warp holding the
+                // group's ragged end stores its valid rows directly, so that no write reaches
+                // the next group's rows.
+                const bool full_warp = c.row0 + quarter * 32 + 32 <= c.row_end;
+                if (lane == 0) tma_store_wait_read();  // the staging boxes are free again
+                __syncwarp();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (h == 1 && !half1) break;
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        pk[i] = static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 64 + 2 * i])) |
-                                (static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 64 + 2 * i + 1])) << 16);
-                    uint4* dst = reinterpret_cast<uint4*>(orow + h * 128 + set * 64);
+                        pk[i] = static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 32 + i].x)) |
+                                (static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 32 + i].y)) << 16);
+                    if (full_warp) {
+                        uint8_t* box = my_stage + h * kOutBox;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(box + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            tma_store_2d(&tmO, box, c.n_tile * kBN + h * 128 + set * 64, c.row0 + quarter * 32);
+                    } else if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + static_cast<int64_t>(row) * p.N +
+                                                              c.n_tile * kBN + h * 128 + set * 64);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                 }
             }
         }
+        if (!p.swiglu && lane == 0) tma_store_wait_all();  // every TMA store has completed
         if (!ok) {
             *abort_flag = 1;
             atomicCAS(&g_tc_error, 0, kErrTimeoutEpilogue);
@@ -327,19 +500,6 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-}
-
-// tile_start[g] = sum over groups before g of ceil(count / 128) * n_tiles_n.
-__global__ void tc_tile_prefix_kernel(int n_groups, int n_tiles_n, const int32_t* __restrict__ offs,
-                                      int32_t* __restrict__ tile_start) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int32_t run = 0;
-    for (int g = 0; g < n_groups; ++g) {
-        tile_start[g] = run;
-        const int32_t cnt = offs[g + 1] - offs[g];
-        run += ((cnt + kBM - 1) / kBM) * n_tiles_n;
-    }
-    tile_start[n_groups] = run;
 }
 
 // ---------------------------------------------------------------- host side
@@ -393,9 +553,7 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 }
 }  // namespace
 
-size_t tc_scratch_bytes(int32_t n_groups) {
-    return (static_cast<size_t>(n_groups) + 1 + 255) / 256 * 1024;
-}
+size_t tc_scratch_bytes(int32_t) { return 0; }
 
 moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N,
                                       int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
@@ -404,34 +562,36 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     const bool swiglu = (epilogue == MOE_EPI_SWIGLU_QUANT);
     if (N % 128 != 0 || (swiglu && N % 256 != 0)) return MOE_ERR_INVALID_ARG;
     if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
-    CUtensorMap tmA, tmB;
+    if (n_groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap tmA, tmB, tmO;
     if (!make_map_u8(&tmA, A, rows, Kd)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tmB, W, static_cast<int64_t>(n_groups) * N, Kd)) return MOE_ERR_CUDA;
-    int32_t* tile_start = static_cast<int32_t*>(ws);
+    if (swiglu) tmO = tmA;  // unused
+    else if (!make_tma_map_2d(&tmO, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, N, 32, 64)) return MOE_ERR_CUDA;
+    (void)ws;  // the tile schedule is built in shared memory
     TcParams p;
     p.n_groups = n_groups;
     p.offs = offs;
-    p.tile_start = tile_start;
     p.N = N;
     p.nkb = Kd / kBK;
+    p.rows = static_cast<int>(rows);
     p.n_tiles_n = swiglu ? (N / 2) / 128 : (N + kBN - 1) / kBN;
     p.swiglu = swiglu ? 1 : 0;
     p.As = As;
     p.Ws = Ws;
     p.out = out;
     p.out_s = out_s;
-    tc_tile_prefix_kernel<<<1, 32, 0, s>>>(n_groups, p.n_tiles_n, offs, tile_start);
-    MOE_LAUNCH_CHECK();
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
+                                        kSmemMax);
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t max_tiles = (ceil_div(rows, kBM) + n_groups) * p.n_tiles_n;
     const int grid = static_cast<int>(max_tiles < device_sm_count() ? max_tiles : device_sm_count());
-    grouped_gemm_fp8_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+    const int smem = kSmemFixed + 4 * (n_groups + 1);
+    grouped_gemm_fp8_tc_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, tmO, p);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -7,7 +7,8 @@
 //   2. scan: offs = exclusive prefix of the counts; base[c][e] = offs[e] + rows of expert e
 //      in chunks before c;
 //   3. positions: inside a chunk, one thread per expert walks the chunk's tokens in order;
-//   4. gather: each destination row copies its token's quantised row (and scales).
+//   4. gather: each destination row copies its token's quantised row; the scales go to a
+//      K-block-major [H/128, R] array, the layout the grouped GEMM reads.
 // With a shared expert, group E follows with every token once, in order.
 #include <mutex>
 
@@ -100,22 +101,41 @@ positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restr
             perm_tok[T * K + t0 + tt] = static_cast<int32_t>(t0 + tt);
 }
 
-// Copy row r of the destination from token perm_tok[r]: row_bytes payload (multiple of 16)
-// and, if scales, n_scales FP32 per row.
-__global__ void __launch_bounds__(128)
+// Copy destination rows [r0, r0 + 32) from their tokens: the row payloads (row_bytes, a
+// multiple of 16, as 16-byte chunks spread over the block) and, if src_s, the n_scales FP32
+// scales of each row, written K-block-major (dst_s[j * R + r]) so that each warp stores 32
+// consecutive rows of one scale column.
+__global__ void __launch_bounds__(256)
 gather_rows_kernel(int64_t R, int64_t T, int64_t row_bytes, int n_scales,
                    const int32_t* __restrict__ perm_tok, const uint8_t* __restrict__ src,
                    const float* __restrict__ src_s, uint8_t* __restrict__ dst,
                    float* __restrict__ dst_s) {
-    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-        const int64_t t = perm_tok[r];
-        if (t < 0 || t >= T) continue;  // a row no valid (token, slot) claimed
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + t * row_bytes);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + r * row_bytes);
-        for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) d4[i] = s4[i];
-        if (src_s)
-            for (int i = threadIdx.x; i < n_scales; i += blockDim.x)
-                dst_s[r * n_scales + i] = src_s[t * n_scales + i];
+    __shared__ int32_t stok[32];
+    const int chunks = static_cast<int>(row_bytes / 16);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    const int64_t n_grp = (R + 31) / 32;
+    for (int64_t gi = blockIdx.x; gi < n_grp; gi += gridDim.x) {
+        const int64_t r0 = gi * 32;
+        const int nr = static_cast<int>(R - r0 < 32 ? R - r0 : 32);
+        __syncthreads();  // the previous group is done with stok
+        if (threadIdx.x < 32) {
+            const int32_t t = threadIdx.x < nr ? perm_tok[r0 + threadIdx.x] : -1;
+            stok[threadIdx.x] = (t >= 0 && t < T) ? t : -1;  // -1: a row no valid (token, slot) claimed
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int i = threadIdx.x; i < nr * chunks; i += blockDim.x) {
+            const int rr = i / chunks, ch = i - rr * chunks;
+            const int64_t t = stok[rr];
+            if (t >= 0) d4[(r0 + rr) * chunks + ch] = s4[t * chunks + ch];
+        }
+        if (src_s) {
+            const int lane = threadIdx.x & 31;
+            const int64_t t = lane < nr ? stok[lane] : -1;
+            for (int j = threadIdx.x >> 5; j < n_scales; j += blockDim.x >> 5)
+                if (t >= 0) dst_s[static_cast<int64_t>(j) * R + r0 + lane] = src_s[t * n_scales + j];
+        }
     }
 }
 
@@ -164,8 +184,9 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     MOE_LAUNCH_CHECK();
     const int64_t R = T * K + T * S;
     const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
-    const int64_t grid = R < 148 * 64 ? R : 148 * 64;
-    gather_rows_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(
+    const int64_t n_grp = ceil_div(R, 32);
+    const int64_t grid = n_grp < 148 * 8 ? n_grp : 148 * 8;
+    gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
         R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
         fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
     MOE_LAUNCH_CHECK();
@@ -240,8 +261,9 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T,
     MOE_LAUNCH_CHECK();
     const int64_t R = T * K + T * S;
     const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
-    const int64_t grid = R < 148 * 64 ? R : 148 * 64;
-    gather_rows_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(
+    const int64_t n_grp = ceil_div(R, 32);
+    const int64_t grid = n_grp < 148 * 8 ? n_grp : 148 * 8;
+    gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
         R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
         fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
     MOE_LAUNCH_CHECK();

@@ -152,7 +152,8 @@ def moe_grouped_gemm_fp8(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue, 
                          stream=None):
     _check("moe_grouped_gemm_fp8", _lib_handle().moe_grouped_gemm_fp8(
         int(n_groups), _ptr(offs), int(rows), int(N), int(Kdim), _ptr(A), _ptr(As), _ptr(W), _ptr(Ws),
-        int(epilogue), _ptr(out), _ptr(out_s), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        int(epilogue), _ptr(out), _ptr(out_s), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_grouped_gemm_f32(n_groups, offs, rows, N, Kdim, A, W, epilogue, out, ws, stream=None):

@@ -148,7 +148,8 @@ MOE_API moe_status moe_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols,
  *  that range is dropped and its row is left unwritten); counts [E]: the gate's histogram,
  *  accepted for symmetry and not read (may be NULL) -- the rows are derived from topk_idx;
  *  FP8 mode: xq [T, H] E4M3 and xs [T, H/128] FP32 (from moe_quant_1x128), gathered into
- *            aq [R, H] and as [R, H/128];
+ *            aq [R, H] and as [H/128, R] (K-block-major: as[j * R + r] is the scale of
+ *            columns 128j..128j+127 of row r, the layout moe_grouped_gemm_fp8 reads);
  *  FP32 mode: xq is x [T, H] FP32 gathered into aq [R, H] FP32; xs and as are ignored.
  *  Outputs: offs [E + 1 + S] int32 (exclusive prefix sum of the rows per group),
  *  perm_tok [R] int32 (token of each row), row_of [T, K] int32 (row of each (t, k)).
@@ -187,11 +188,14 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T, const i
  *  n_groups >= 1; offs [n_groups + 1] device int32, non-decreasing, offs[0] == 0,
  *  offs[n_groups] <= rows; rows = capacity (host) of A and out; N % 128 == 0 (for
  *  SWIGLU_QUANT, N = 2I with I % 128 == 0); Kdim % 128 == 0.
- *  A [rows, Kdim] E4M3, As [rows, Kdim/128]; W [n_groups, N, Kdim] E4M3,
- *  Ws [n_groups, N/128, Kdim/128];
- *  SWIGLU_QUANT: out [rows, N/2] E4M3 and out_s [rows, N/256] FP32 (the 1x128 quantisation
- *  of h in FP32 -> FP8, no intermediate rounding); STORE: out [rows, N] BF16, out_s unused.
- *  Rows beyond offs[n_groups] are left untouched.  16-byte aligned pointers. */
+ *  A [rows, Kdim] E4M3, As [Kdim/128, rows] (K-block-major: As[kb * rows + r]);
+ *  W [n_groups, N, Kdim] E4M3, Ws [n_groups, N/128, Kdim/128];
+ *  SWIGLU_QUANT: out [rows, N/2] E4M3 and out_s [N/256, rows] FP32, K-block-major like As
+ *  (the 1x128 quantisation of h in FP32 -> FP8, no intermediate rounding);
+ *  STORE: out [rows, N] BF16, out_s unused.
+ *  Rows beyond offs[n_groups] are left untouched.  16-byte aligned pointers.
+ *  n_groups <= 2048 (MOE_ERR_UNSUPPORTED beyond).  ws/ws_bytes are not used (the tile
+ *  schedule is built in shared memory from offs); they may be NULL/0. */
 MOE_API moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, int64_t rows,
                                 int32_t N, int32_t Kdim, const uint8_t* A, const float* As,
                                 const uint8_t* W, const float* Ws, int32_t epilogue,

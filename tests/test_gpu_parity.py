@@ -164,14 +164,14 @@ def test_permute_bitexact(moe, orc, T, E, K, S):
     perm_tok = torch.empty(R, dtype=torch.int32, device=DEV)
     row_of = torch.empty(T, K, dtype=torch.int32, device=DEV)
     aq = torch.empty(R, H, dtype=torch.uint8, device=DEV)
-    as_ = torch.empty(R, H // 128, dtype=torch.float32, device=DEV)
+    as_ = torch.empty(H // 128, R, dtype=torch.float32, device=DEV)  # K-block-major
     ws = moe.workspace(cfg, T)
     moe.moe_permute(cfg, T, d_idx, counts, xq, xs, offs, perm_tok, row_of, aq, as_, ws)
     torch.cuda.synchronize()
     ref = check_permutation(dict(offs=to_host(offs), perm_tok=to_host(perm_tok), row_of=to_host(row_of)),
                             idx, orc, E, S)
     assert np.array_equal(to_host(aq), to_host(xq)[ref["perm_tok"]])
-    assert np.array_equal(to_host(as_), to_host(xs)[ref["perm_tok"]])
+    assert np.array_equal(to_host(as_), to_host(xs)[ref["perm_tok"]].T)
 
 
 # ------------------------------------------------------------------ grouped expert GEMMs
@@ -197,13 +197,14 @@ def test_grouped_gemm_fp8_swiglu_and_down(moe, orc, H, I, E, R):
     aq = torch.empty(R, H, dtype=torch.uint8, device=DEV)
     as_ = torch.empty(R, H // 128, dtype=torch.float32, device=DEV)
     moe.moe_quant_1x128(x.view(torch.uint16), aq, as_)
+    as_k = as_.t().contiguous()  # the GEMM reads K-block-major scales
     qw = moe.quantize_weights(W13, W2)
     d_offs = torch.from_numpy(offs).to(DEV)
     hq = torch.empty(R, I, dtype=torch.uint8, device=DEV)
-    hs = torch.empty(R, I // 128, dtype=torch.float32, device=DEV)
+    hs = torch.empty(I // 128, R, dtype=torch.float32, device=DEV)  # written K-block-major
     ws = torch.empty(64 << 20 if R * 2 * I * 4 < (60 << 20) else R * 2 * I * 4 + (4 << 20),
                      dtype=torch.uint8, device=DEV)
-    moe.moe_grouped_gemm_fp8(E, d_offs, R, 2 * I, H, aq, as_, qw["W13"], qw["W13_s"],
+    moe.moe_grouped_gemm_fp8(E, d_offs, R, 2 * I, H, aq, as_k, qw["W13"], qw["W13_s"],
                              moe.MOE_EPI_SWIGLU_QUANT, hq, hs, ws)
     y = torch.empty(R, H, dtype=torch.bfloat16, device=DEV)
     moe.moe_grouped_gemm_fp8(E, d_offs, R, H, I, hq, hs, qw["W2"], qw["W2_s"], moe.MOE_EPI_STORE,
@@ -215,10 +216,11 @@ def test_grouped_gemm_fp8_swiglu_and_down(moe, orc, H, I, E, R):
     oq = orc.quantize_weights(to_host(W13), to_host(W2))
     yref, aux = orc.ffn_fp8(rq, rs, row_e, *oq, want_h=True)
     table = orc.e4m3_table()
-    h_gpu = table[to_host(hq)] * np.repeat(to_host(hs), 128, axis=1)
+    hs_rows = to_host(hs).T
+    h_gpu = table[to_host(hq)] * np.repeat(hs_rows, 128, axis=1)
     h_ref = aux["h"].astype(np.float64)
     # GEMM1 + SwiGLU + 1x128 quantisation: within one code step of the oracle's FP32 h
-    assert np.allclose(to_host(hs), aux["hs"], rtol=1e-5, atol=0)
+    assert np.allclose(hs_rows, aux["hs"], rtol=1e-5, atol=0)
     step = np.repeat(aux["hs"], 128, axis=1) * 32.0  # largest E4M3 step (256..448) in code units
     assert np.all(np.abs(h_gpu - h_ref) <= step * 0.5 + 1e-30)
     # the codes themselves agree except where h sits on a rounding boundary (FP32 sums in

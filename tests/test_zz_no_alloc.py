@@ -45,7 +45,7 @@ def _outputs(cfg, T):
                 perm_tok=torch.full((R,), -1, dtype=torch.int32, device=DEV),
                 row_of=torch.full((T, K), -1, dtype=torch.int32, device=DEV),
                 aq=torch.zeros(R, 512, dtype=torch.uint8, device=DEV),
-                as_=torch.zeros(R, 4, dtype=torch.float32, device=DEV))
+                as_=torch.zeros(4, R, dtype=torch.float32, device=DEV))  # K-block-major
 
 
 def test_noalloc_matches_workspace_permute_on_two_calls(moe):
