@@ -13,9 +13,10 @@
 //               per 128-wide K block into a 3-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates 512 TMEM columns; one lane issues 4 MMAs (K = 32 each) per K block
 //               into one of two 256-column FP32 partial buffers, then commits;
-//   warps 2-3   scale loaders: for each K block, the tile's 128 activation scales and its two
-//               weight scales go into a 4-slot shared-memory ring, so that the promotion warps
-//               issue no global loads (a pending global load stalls their tcgen05 fences);
+//   warp 2      scale loader: for each K block, the tile's 128 activation scales and its two
+//               weight scales go into a 16-slot shared-memory ring by asynchronous copies, so
+//               that the promotion warps issue no global loads (a pending global load stalls
+//               their tcgen05 fences); warp 3 idles;
 //   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld, 16 columns at a
 //               time with the next load in flight), scale it by as[kb,r] * Ws[g,nb,kb] into
 //               FP32 register pairs (packed FP32x2 FMA), release the buffer; after the last
@@ -47,20 +48,23 @@ constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2-3 scales, warps 4..11 epilogue
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2 scales, 3 idle, 4..11 epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
-constexpr int kMaxGroups = 2048;
+constexpr int kMaxGroups = 1040;
 constexpr int kOutBox = 32 * 128;                       // one warp's 32 rows x 128 B of output
 constexpr int kOutBytes = kEpiWarps * 2 * kOutBox;      // two staging boxes per epilogue warp
-constexpr int kScaleSlots = 4;
-constexpr int kSlotFloats = 136;  // 128 activation scales, 2 weight scales, padding to 16 bytes
+constexpr int kScaleSlots = 16;  // K blocks of scale copies in flight (covers L2 latency under load)
+constexpr int kSlotFloats = 132;  // 128 activation scales, 2 weight scales, padding to 16 bytes
 // Control block after the operand ring and the output staging (byte offsets): barriers,
 // TMEM address and flags, amax exchange, warp sums, scale ring, then the tile prefix.
-constexpr int kCtlBars = 0, kCtlSlot = 256, kCtlRed = 272, kCtlWarpSums = kCtlRed + 2048,
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 2 * kScaleSlots;  // full/empty, pfull/pempty,
+                                                                      // mma_done, ebar, sfull/sempty
+constexpr int kCtlBars = 0, kCtlSlot = (kNumBars * 8 + 15) / 16 * 16, kCtlRed = kCtlSlot + 16,
+              kCtlWarpSums = kCtlRed + 2048,
               kCtlScales = kCtlWarpSums + 64, kCtlTiles = kCtlScales + kScaleSlots * kSlotFloats * 4;
 constexpr int kSmemFixed = 1024 + kStages * kStageBytes + kOutBytes + kCtlTiles;
 constexpr int kSmemMax = kSmemFixed + 4 * (kMaxGroups + 1);
@@ -114,6 +118,17 @@ __device__ __forceinline__ void scale_add16(float2 (&acc)[64], int base, const f
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[base + i] = __ffma2_rn(make_float2(r[2 * i], r[2 * i + 1]), s, acc[base + i]);
 }
+
+// 4-byte asynchronous global -> shared copy (L1-allocating; the data is read once per CTA).
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the arrival is
+// one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 2D TMA store of a [32 rows x 128 B] box from shared memory (128-byte swizzle) at (x, y).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
@@ -192,6 +207,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint64_t* ebar = mma_done + 1;          // [1]        epilogue amax exchange (one phase per tile)
     uint64_t* sfull = ebar + 1;             // [kScaleSlots] scale loaders -> epilogue
     uint64_t* sempty = sfull + kScaleSlots; // [kScaleSlots] epilogue -> scale loaders
+    static_assert(2 * kStages + 6 + 2 * kScaleSlots <= kNumBars, "barrier block");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + kCtlSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;   // stays 0: drains wait for in-flight work, not for aborts
@@ -213,7 +229,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         mbar_init(mma_done, 1);
         mbar_init(ebar, kEpiThreads);
         for (int i = 0; i < kScaleSlots; ++i) {
-            mbar_init(&sfull[i], 1);
+            mbar_init(&sfull[i], 32);
             mbar_init(&sempty[i], kEpiWarps);
         }
         *abort_flag = 0;
@@ -233,8 +249,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int total = tile_start[p.n_groups];
 
     if (warp < kEpiWarp0) {
-        // register split: 4 x 40 (TMA, MMA, 2 scale loaders) + 8 x 232 (epilogue) = 12 x 168
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+        // register split: 4 x 48 (TMA, MMA, scale loader, idle) + 8 x 224 (epilogue) <= 12 x 168
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 48;");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------------- producer
             int s = 0;
@@ -300,53 +316,49 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             // drain: every MMA this thread issued has completed once mma_done flips
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, never, kWaitBudget);
-        } else if (warp == 2 || warp == 3) {
-            // ---------------------------------------------------------------- scale loaders
-            // Warp 2 fills the slots of the even K-block counts, warp 3 the odd ones; each warp
-            // loads its next block's scales into registers while it waits for the slot.
-            const int my_tiles = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-            const int kc_total = my_tiles * p.nkb;
-            float v[4], w0 = 0.f, w1 = 0.f;
-            auto fetch = [&](int kc) {
-                const TileCoord c = decode_tile(p, tile_start, blockIdx.x + (kc / p.nkb) * gridDim.x);
-                const int kb = kc % p.nkb;
-                const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = c.row0 + lane + 32 * j;
-                    v[j] = r < c.row_end ? __ldg(col + r) : 0.f;
-                }
-                const int64_t nbk = p.N / 128;
-                const int b1 = b_block(p, c, 1);
-                w0 = __ldg(p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb + kb);
-                w1 = b1 < nbk ? __ldg(p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb + kb) : 0.f;
-            };
+        } else if (warp == 2) {
+            // ---------------------------------------------------------------- scale loader
+            // For each K block, once the ring slot is free: every lane copies four activation
+            // scales and lane 0 the two weight scales with asynchronous 4-byte global->shared
+            // copies, then each lane's copies arrive on the slot's barrier when they land
+            // (cp.async.mbarrier.arrive.noinc; 32 arrivals complete the phase).  Up to
+            // kScaleSlots blocks of copies are in flight.  Rows past the group's end and the
+            // absent second weight block copy a valid neighbour: those values are never stored.
             uint32_t sph = 0;  // bit i: parity of the next use of slot i
             bool ok = true;
-            int kc = warp & 1;
-            if (kc < kc_total) fetch(kc);
-            for (; kc < kc_total; kc += 2) {
-                const int i = kc % kScaleSlots;
-                if (!mbar_wait(&sempty[i], ((sph >> i) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
-                sph ^= 1u << i;
-                float* slot = sring + i * kSlotFloats;
+            int kc = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile(p, tile_start, t);
+                const int64_t nbk = p.N / 128;
+                const int b1 = b_block(p, c, 1);
+                const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb;
+                const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
+                for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
+                    const int i = kc % kScaleSlots;
+                    if (!mbar_wait(&sempty[i], ((sph >> i) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                    sph ^= 1u << i;
+                    float* slot = sring + i * kSlotFloats;
+                    const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) slot[lane + 32 * j] = v[j];
-                if (lane == 0) {
-                    slot[128] = w0;
-                    slot[129] = w1;
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = c.row0 + lane + 32 * j;
+                        cp_async4(slot + lane + 32 * j, col + (r < c.row_end ? r : c.row0));
+                    }
+                    if (lane == 0) {
+                        cp_async4(slot + 128, ws0 + kb);
+                        cp_async4(slot + 129, ws1 + kb);
+                    }
+                    cp_async_mbar_arrive(&sfull[i]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sfull[i]);
-                if (kc + 2 < kc_total) fetch(kc + 2);
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicCAS(&g_tc_error, 0, kErrTimeoutScales);
             }
+            cp_async_wait_all();  // nothing in flight when the CTA exits
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
         // -------------------------------------------------------------------- promotion + epilogue
         // 128 FP32 accumulators per thread (64 pairs) plus two 16-column TMEM staging chunks.
         const int ew = warp - kEpiWarp0;       // 0..7

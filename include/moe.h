@@ -194,7 +194,7 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T, const i
  *  (the 1x128 quantisation of h in FP32 -> FP8, no intermediate rounding);
  *  STORE: out [rows, N] BF16, out_s unused.
  *  Rows beyond offs[n_groups] are left untouched.  16-byte aligned pointers.
- *  n_groups <= 2048 (MOE_ERR_UNSUPPORTED beyond).  ws/ws_bytes are not used (the tile
+ *  n_groups <= 1040 (MOE_ERR_UNSUPPORTED beyond).  ws/ws_bytes are not used (the tile
  *  schedule is built in shared memory from offs); they may be NULL/0. */
 MOE_API moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, int64_t rows,
                                 int32_t N, int32_t Kdim, const uint8_t* A, const float* As,
