@@ -57,6 +57,11 @@ _SIGS = {
     "moe_forward": [_cfgp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp,
                     _vp, _vp, _sz, _vp],
     "moe_device_error": [ctypes.POINTER(_i32)],
+    "moe_pipeline_workspace_size": [_cfgp, _i64, ctypes.POINTER(_sz)],
+    "moe_pipeline_create": [_cfgp, _i64, _vp, _sz, _vp, ctypes.POINTER(_vp)],
+    "moe_pipeline_submit": [_vp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp, _vp],
+    "moe_pipeline_wait": [_vp],
+    "moe_pipeline_destroy": [_vp],
 }
 
 
@@ -225,3 +230,60 @@ def quantize_weights(W13, W2, stream=None):
         moe_quant_128x128(W.view(torch.uint16) if W.dtype == torch.bfloat16 else W, q, s, stream)
         out[name], out[name + "_s"] = q, s
     return out
+
+
+# ---------------------------------------------------------------- host-buffer pipeline
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("moe_pipeline_submit takes host tensors; got a %s tensor" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def moe_pipeline_workspace_size(cfg, max_T):
+    n = _sz(0)
+    _check("moe_pipeline_workspace_size", _lib_handle().moe_pipeline_workspace_size(
+        ctypes.byref(_cfg(cfg)), int(max_T), ctypes.byref(n)))
+    return n.value
+
+
+class MoEPipeline:
+    """moe_pipeline_create / submit / wait / destroy: the layer from and to (pinned) host
+    tensors, with consecutive batches' copies overlapping each other's compute."""
+
+    def __init__(self, cfg, max_T, ws=None, stream=None, device="cuda"):
+        self.cfg = _cfg(cfg)
+        self.ws = ws if ws is not None else torch.empty(
+            (moe_pipeline_workspace_size(cfg, max_T),), dtype=torch.uint8, device=device)
+        self.handle = _vp(0)
+        _check("moe_pipeline_create", _lib_handle().moe_pipeline_create(
+            ctypes.byref(self.cfg), int(max_T), _ptr(self.ws), self.ws.numel() * self.ws.element_size(),
+            _stream(stream), ctypes.byref(self.handle)))
+        self._keep = []
+
+    def submit(self, x_host, weights, bias, update_bias, y_host, topk_idx_host, topk_w_host, counts_host):
+        w = moe_weights(_ptr(weights["Wg"]), _ptr(weights["W13"]), _ptr(weights.get("W13_s")),
+                        _ptr(weights["W2"]), _ptr(weights.get("W2_s")))
+        self._keep = [w]
+        _check("moe_pipeline_submit", _lib_handle().moe_pipeline_submit(
+            self.handle, int(x_host.shape[0]), _host_ptr(x_host), ctypes.byref(w), _ptr(bias),
+            int(update_bias), _host_ptr(y_host), _host_ptr(topk_idx_host), _host_ptr(topk_w_host),
+            _host_ptr(counts_host)))
+
+    def wait(self):
+        _check("moe_pipeline_wait", _lib_handle().moe_pipeline_wait(self.handle))
+
+    def close(self):
+        if self.handle:
+            _check("moe_pipeline_destroy", _lib_handle().moe_pipeline_destroy(self.handle))
+            self.handle = _vp(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -237,6 +237,37 @@ MOE_API moe_status moe_forward(const moe_config* cfg, int64_t T, const void* x, 
                        float* topk_w, int32_t* counts, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* The layer forward from and to HOST memory, pipelined across batches (a serving loop's
+ * shape; the pages' layer has no host interface, this is a library convenience).  Each
+ * batch's tokens are uploaded on a copy stream, run through moe_forward on the caller's
+ * stream and its outputs downloaded on a second copy stream, so that batch n+1's upload and
+ * batch n-1's download overlap batch n's compute.  Two device slots alternate between
+ * consecutive batches; batches compute in submission order (a bias update by batch n is seen
+ * by batch n+1).
+ *  Ownership: the caller allocates the device workspace (moe_pipeline_workspace_size bytes
+ *  for batches of up to max_T tokens, 16-byte aligned) and keeps it, the weights and the
+ *  bias alive until moe_pipeline_destroy; the pipeline object owns two CUDA streams and a few
+ *  events (host-side handles) and no device memory.  Work enqueued on `stream` before
+ *  moe_pipeline_create completes before the pipeline touches the workspace.
+ *  Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
+ *  be asynchronous; a submit returns once its work is enqueued, and the host buffers of a
+ *  batch may be reused after moe_pipeline_wait (or once later batches' waits show it done).
+ *  Errors: MOE_ERR_INVALID_ARG (bad pointer or T > max_T), MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
+typedef struct moe_pipeline moe_pipeline;
+MOE_API moe_status moe_pipeline_workspace_size(const moe_config* cfg, int64_t max_T, size_t* bytes);
+MOE_API moe_status moe_pipeline_create(const moe_config* cfg, int64_t max_T, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream, moe_pipeline** out);
+/* x_host [T, H] (BF16 / FP32 by mode); outputs y_host [T, H], topk_idx_host [T, K],
+ * topk_w_host [T, K], counts_host [E] (the batch's histogram), all host memory; w and bias
+ * as for moe_forward (device). */
+MOE_API moe_status moe_pipeline_submit(moe_pipeline* pl, int64_t T, const void* x_host, const moe_weights* w,
+                                       float* bias, int32_t update_bias, void* y_host, int32_t* topk_idx_host,
+                                       float* topk_w_host, int32_t* counts_host);
+/* Blocks the host until every submitted batch's outputs are in host memory. */
+MOE_API moe_status moe_pipeline_wait(moe_pipeline* pl);
+/* Waits for the pipeline's work, then releases its streams and events (NULL: no-op). */
+MOE_API moe_status moe_pipeline_destroy(moe_pipeline* pl);
+
 /* Device-side error word written by bounded waits inside the kernels (0 = none).  Reading
  * it synchronises the device.  *code receives the word; the call then clears it. */
 MOE_API moe_status moe_device_error(int32_t* code);

@@ -86,3 +86,27 @@ def test_host_side_argument_checks(moe):
                          vp(16), vp(16), vp(16), vp(16), need.value - 1, None) == moe.MOE_ERR_WORKSPACE
     assert L.moe_workspace_size(ctypes.byref(cfg), -1, ctypes.byref(need)) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_status_string(moe.MOE_ERR_TIMEOUT).startswith(b"MOE_ERR_TIMEOUT")
+
+
+def test_pipeline_host_side_checks(moe):
+    L = moe._lib_handle()
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    cfg = moe.make_config(sy.config("v3_prefill"))
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.moe_pipeline_workspace_size(ctypes.byref(cfg), 1000, ctypes.byref(a)) == moe.MOE_OK
+    assert L.moe_pipeline_workspace_size(ctypes.byref(cfg), 2000, ctypes.byref(b)) == moe.MOE_OK
+    layer = ctypes.c_size_t(0)
+    assert L.moe_workspace_size(ctypes.byref(cfg), 1000, ctypes.byref(layer)) == moe.MOE_OK
+    # the layer workspace plus two slots of x and y (BF16 [T, H]) at least
+    assert a.value >= layer.value + 4 * 1000 * 7168 * 2 and b.value > a.value
+    assert L.moe_pipeline_workspace_size(ctypes.byref(cfg), 0, ctypes.byref(a)) == moe.MOE_ERR_INVALID_ARG
+    h = ctypes.c_void_p(0)
+    # rejected before any CUDA call: no workspace, a misaligned one, one too small
+    assert L.moe_pipeline_create(ctypes.byref(cfg), 1000, None, b.value, None, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_create(ctypes.byref(cfg), 1000, ctypes.c_void_p(17), b.value, None,
+                                 ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_create(ctypes.byref(cfg), 1000, ctypes.c_void_p(16), 100, None,
+                                 ctypes.byref(h)) == moe.MOE_ERR_WORKSPACE
+    assert not h.value
+    assert L.moe_pipeline_submit(None, 1, None, None, None, 0, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_destroy(None) == moe.MOE_OK
