@@ -9,8 +9,9 @@
 // Two kernels:
 //  - gate_tc_kernel (BF16 x and Wg, E <= 256): the [128 tokens x E] logit tile is one
 //    tcgen05 MMA accumulation in TMEM (BF16 x BF16 products are exact in FP32, FP32
-//    accumulation), fed by TMA; then one thread per token reads its logits back from TMEM
-//    and runs the selection in registers.  The kernel streams x once: HBM-bound.
+//    accumulation), fed by TMA; then all 8 warps run the selection, two threads per token
+//    (each reads half of the token's groups from TMEM, the pair exchanges group scores and
+//    merges two local top-k lists through shared memory).  The kernel streams x once.
 //  - gate_fused_kernel (FP32 inputs, or shapes outside the tensor-core kernel's range): the
 //    [kTok, E] logit tile is formed in shared memory on the CUDA cores, then each warp runs
 //    the selection for its tokens with warp shuffles (lane l holds experts l, l+32, ...).
@@ -215,7 +216,8 @@ gate_fused_kernel(int64_t Tn, int H, int E, int G, int TG, int K, float rsf,
 constexpr int kGtM = 128;           // tokens per CTA (MMA M)
 constexpr int kGtK = 64;            // BF16 columns per stage (128 bytes: one swizzle row)
 constexpr int kGtStages = 4;
-constexpr int kGtThreads = 256;     // warp 0 TMA, warp 1 MMA + TMEM, warps 4..7 selection
+constexpr int kGtThreads = 512;     // warp 0 TMA, warp 1 MMA + TMEM; all 16 warps select
+constexpr int kGtParts = kGtThreads / 128;  // threads per token in pass 1
 constexpr int kGtMaxE = 256;
 constexpr int kGtMaxK = 8;
 constexpr int kGtMaxG = 8;
@@ -236,6 +238,11 @@ struct GateTcParams {
     float* topk_w;
     int32_t* counts;
 };
+
+// sigmoid with the fast exponential and division intrinsics (a few ulp in FP32; the selection
+// is compared with the exact scores only where its margin exceeds 1e-5, and the weights within
+// 2e-5 of the routing scale).  x -> -inf gives 0, x -> +inf gives 1.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __global__ void __launch_bounds__(kGtThreads, 1)
 gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -330,107 +337,112 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             }
             mma_commit(acc_full);  // fires when every MMA above has completed
         }
-    } else if (warp >= 4) {
-        // -------------------------------------------------------------- selection, one token per thread
-        const int quarter = warp & 3;
-        const int64_t t = t0 + quarter * 32 + lane;
-        const bool ok = mbar_wait(acc_full, 0, abort_flag, kGtWaitBudget);
+    }
+    __syncwarp();  // the producer and MMA lanes rejoin their warps
+    // ------------------------------------------------------------------ selection, all warps
+    // Pass 1, one thread per (token, part of its groups): warp w reads TMEM lanes 32*(w % 4)..
+    // (its tokens) and computes the group scores of part w / 4 of the groups, storing them and
+    // the logits in the operand ring, idle once every MMA has completed.
+    {
+        const int quarter = warp & 3, h = warp >> 2;  // h: which part of the token's groups
+        const int tl = quarter * 32 + lane;
+        bool ok = mbar_wait(acc_full, 0, abort_flag, kGtWaitBudget);
+        ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
         tc_fence_after();
-        if (!ok) {
+        if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicCAS(&g_gate_error, 0, 0x203);
-        } else {
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            const int gsz = p.E / p.G;   // a multiple of 32: each 32-column chunk lies in one group
-            const int cpg = gsz / 32;
-            float gs[kGtMaxG];
-            // pass 1: group scores = sum of the two largest selection scores of each group
-            for (int g = 0; g < kGtMaxG; ++g) {
-                float a1 = -INFINITY, a2 = -INFINITY;
-                if (g < p.G) {
-                    for (int cc = 0; cc < cpg; ++cc) {
-                        float l[32];
-                        tmem_ld32(taddr + (g * cpg + cc) * 32, l);
-                        tmem_ld_wait_regs(l);
+        }
+        float* gsc = reinterpret_cast<float*>(smem);          // [kGtM][kGtMaxG] group scores
+        float* lg = gsc + kGtM * kGtMaxG;                      // [kGtM][E + 1] logits (padded row)
+        const int lgs = p.E + 1;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int gsz = p.E / p.G;   // a multiple of 32: each 32-column chunk lies in one group
+        const int cpg = gsz / 32;
+        const int gper = (p.G + kGtParts - 1) / kGtParts;
+        const int g_lo = min(h * gper, p.G), g_hi = min(g_lo + gper, p.G);
+        // pass 1: group score = sum of the two largest selection scores of the group
+        for (int g = g_lo; g < g_hi && ok; ++g) {
+            float a1 = -INFINITY, a2 = -INFINITY;
+            for (int cc = 0; cc < cpg; ++cc) {
+                float l[32];
+                tmem_ld32(taddr + (g * cpg + cc) * 32, l);
+                tmem_ld_wait_regs(l);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float sv = 1.0f / (1.0f + expf(-l[j]));
-                            const float c = sv + sbias[(g * cpg + cc) * 32 + j];
-                            if (c > a1) { a2 = a1; a1 = c; } else if (c > a2) { a2 = c; }
-                        }
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const float c = sigmoid_fast(l[j]) + sbias[(g * cpg + cc) * 32 + j];
+                    if (c > a1) { a2 = a1; a1 = c; } else if (c > a2) { a2 = c; }
+                    lg[tl * lgs + (g * cpg + cc) * 32 + j] = l[j];  // (tl + e) % 32 banks: no conflicts
                 }
-                gs[g] = a1 + a2;
             }
-            // keep topk_group groups (ties to the lower index)
+            gsc[tl * kGtMaxG + g] = a1 + a2;
+        }
+        __syncthreads();
+        // pass 2, one warp per token (warp w takes tokens w, w + 16, ...): lane l holds experts
+        // l + 32 j; keep topk_group groups by the group scores, then top_k rounds of a
+        // warp arg-max over the kept experts' selection scores (ties to the lower index, slots
+        // in descending score).  The un-biased scores are recomputed from the stored logits
+        // with the same instructions as in pass 1.
+        const int epl = p.E / 32;
+        for (int tok = warp; tok < kGtM && ok; tok += kGtThreads / 32) {
+            const int64_t tt = t0 + tok;
+            if (tt >= p.T) break;
             uint32_t kept = 0;
             for (int r = 0; r < p.TG; ++r) {
                 int best = -1;
                 float bv = -INFINITY;
-#pragma unroll
-                for (int g = 0; g < kGtMaxG; ++g)
-                    if (g < p.G && !((kept >> g) & 1u) && (best < 0 || gs[g] > bv)) { best = g; bv = gs[g]; }
+                for (int g = 0; g < p.G; ++g) {
+                    const float v = gsc[tok * kGtMaxG + g];
+                    if (!((kept >> g) & 1u) && (best < 0 || v > bv)) { best = g; bv = v; }
+                }
                 kept |= 1u << (best < 0 ? 0 : best);
             }
-            // pass 2: top_k experts among the kept groups, in ascending expert order so that an
-            // equal score never displaces an earlier (lower-index) expert
-            float tv[kGtMaxK], ts[kGtMaxK];
-            int ti[kGtMaxK];
+            uint32_t skept = 0;  // bit j: slot j (group j / cpg) is in a kept group
+            for (int j = 0; j < epl; ++j)
+                if ((kept >> (j / cpg)) & 1u) skept |= 1u << j;
+            float sv[kGtMaxE / 32], cv[kGtMaxE / 32];
 #pragma unroll
-            for (int k = 0; k < kGtMaxK; ++k) { tv[k] = -INFINITY; ts[k] = 0.f; ti[k] = 0x7fffffff; }
-            // (every lane loads every chunk: tcgen05.ld is warp-collective; the group test only
-            // predicates the per-token processing)
-            for (int g = 0; g < p.G; ++g) {
-                const bool keep = (kept >> g) & 1u;
-                for (int cc = 0; cc < cpg; ++cc) {
-                    float l[32];
-                    tmem_ld32(taddr + (g * cpg + cc) * 32, l);
-                    tmem_ld_wait_regs(l);
-                    if (!keep) continue;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int e = (g * cpg + cc) * 32 + j;
-                        const float sv = 1.0f / (1.0f + expf(-l[j]));
-                        const float c = sv + sbias[e];
-                        // current K-th entry (compile-time indexing keeps the list in registers)
-                        float kv = -INFINITY;
-                        bool kfull = false;
-#pragma unroll
-                        for (int k = 0; k < kGtMaxK; ++k)
-                            if (k == p.K - 1) { kv = tv[k]; kfull = ti[k] != 0x7fffffff; }
-                        if (!kfull || c > kv) {
-                            // insert after every entry >= c
-                            float cv = c, cs = sv;
-                            int ci = e;
-#pragma unroll
-                            for (int k = 0; k < kGtMaxK; ++k) {
-                                if (k < p.K && (ti[k] == 0x7fffffff || cv > tv[k])) {
-                                    const float xv = tv[k], xs = ts[k];
-                                    const int xi = ti[k];
-                                    tv[k] = cv; ts[k] = cs; ti[k] = ci;
-                                    cv = xv; cs = xs; ci = xi;
-                                }
-                            }
-                        }
-                    }
+            for (int j = 0; j < kGtMaxE / 32; ++j) {
+                const int e = lane + 32 * j;
+                cv[j] = -INFINITY;
+                sv[j] = 0.f;
+                if ((skept >> j) & 1u) {
+                    sv[j] = sigmoid_fast(lg[tok * lgs + e]);
+                    cv[j] = sv[j] + sbias[e];
                 }
             }
-            if (t < p.T) {
-                float den = 0.f;
+            uint32_t taken = 0;
+            float den = 0.f, my_w = 0.f;
+            int my_e = 0;
+            for (int k = 0; k < p.K; ++k) {
+                float v = -INFINITY, s_best = 0.f;
+                int i = 0x7fffffff;
 #pragma unroll
-                for (int k = 0; k < kGtMaxK; ++k)
-                    if (k < p.K) den = den + ts[k];
-                if (p.K > 1) den = den + 1e-20f;
-#pragma unroll
-                for (int k = 0; k < kGtMaxK; ++k) {
-                    if (k < p.K) {
-                        const int e = (ti[k] >= 0 && ti[k] < p.E) ? ti[k] : 0;
-                        const float w = (p.K > 1) ? ts[k] / den : ts[k];
-                        p.topk_idx[t * p.K + k] = e;
-                        p.topk_w[t * p.K + k] = w * p.rsf;
-                        atomicAdd(&shist[e], 1);
+                for (int j = 0; j < kGtMaxE / 32; ++j) {
+                    const int e = lane + 32 * j;
+                    if (((skept & ~taken) >> j) & 1u && (cv[j] > v || (cv[j] == v && e < i))) {
+                        v = cv[j]; i = e; s_best = sv[j];
                     }
                 }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+                }
+                if (i >= p.E) i = 0;  // no candidate (NaN scores): expert 0, never out of range
+                const int owner = i & 31;
+                if (lane == owner) taken |= 1u << (i >> 5);
+                const float sw = __shfl_sync(0xffffffffu, s_best, owner);
+                den = den + sw;
+                if (lane == k) { my_w = sw; my_e = i; }
+            }
+            if (p.K > 1) den = den + 1e-20f;
+            if (lane < p.K) {
+                const float w = (p.K > 1) ? my_w / den : my_w;
+                p.topk_idx[tt * p.K + lane] = my_e;
+                p.topk_w[tt * p.K + lane] = w * p.rsf;
+                atomicAdd(&shist[my_e], 1);
             }
         }
     }

@@ -458,9 +458,10 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (h == 1 && !half1) break;
                     uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pk[i] = static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 32 + i].x)) |
-                                (static_cast<uint32_t>(f32_to_bf16_bits(acc[h * 32 + i].y)) << 16);
+                    for (int i = 0; i < 32; ++i) {  // one paired round-to-nearest-even conversion
+                        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[h * 32 + i].x, acc[h * 32 + i].y);
+                        pk[i] = *reinterpret_cast<const uint32_t*>(&v);
+                    }
                     if (full_warp) {
                         uint8_t* box = my_stage + h * kOutBox;
 #pragma unroll
