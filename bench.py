@@ -27,6 +27,9 @@ sys.path.insert(0, ROOT)
 from fp8_gemm_sigmoid_b300 import moe, synthetic as sy  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gate": "gate.cu",
+                  "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu"}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 # kernels each entry point launches (memsets excluded); summed into gpu_launches
@@ -51,6 +54,8 @@ def parse():
     p.add_argument("--experts", type=int, default=None)
     p.add_argument("--groups", type=int, default=None)
     p.add_argument("--topk-group", type=int, default=None)
+    # one stage alone (a profiler's target with a small device footprint)
+    p.add_argument("--only", choices=["gate"], default=None)
     return p.parse_args()
 
 
@@ -194,6 +199,25 @@ def stage_work(cfg):
     }
 
 
+def measured_traffic(stage, workload):
+    """DRAM bytes (read + write) of one launch of the stage's kernel, from the ncu counters in
+    profiles/dram_traffic.txt, or None when none were taken for this workload or the kernel's
+    source has changed since (the file records the source's SHA-256)."""
+    import hashlib
+    src = KERNEL_SOURCES.get(stage)
+    if src is None or not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(os.path.join(ROOT, "fp8_gemm_sigmoid_b300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 5 and not line.startswith("#") and parts[0] == workload and parts[1] == stage:
+                if parts[2] == sha:
+                    return int(parts[3]) + int(parts[4])
+    return None
+
+
 def barrier_sync(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -271,6 +295,31 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args, cfg):
+    """moe_gate alone on the workload's tokens: K timed calls after W warm-up calls."""
+    torch.cuda.set_device(0)
+    T = cfg["T"]
+    inp = sy.make_inputs(cfg, "cuda", weights=False)
+    out = moe.empty_outputs(cfg, T)
+    fp8 = cfg["mode"] == "fp8"
+    x = inp["x"].view(torch.uint16) if fp8 else inp["x"]
+    Wg = inp["Wg"].view(torch.uint16) if fp8 else inp["Wg"]
+    call = lambda: moe.moe_gate(cfg, x, Wg, inp["bias"], out["topk_idx"], out["topk_w"], out["counts"])  # noqa: E731
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    nbytes = stage_work(cfg)["gate"][1]
+    print(json.dumps({"stage": "gate", "workload": cfg["name"], "T": T, "us_per_call": ms * 1e3,
+                      "GB/s": nbytes / ms / 1e6, "steps": args.steps}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -279,6 +328,8 @@ def main():
     over = {k: v for k, v in (("T", args.T), ("n_experts", args.experts), ("n_group", args.groups),
                               ("topk_group", args.topk_group)) if v is not None}
     cfg = sy.config(args.config, **over)
+    if args.only:
+        return run_only(args, cfg)
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
     dist_on = world > 1
@@ -386,7 +437,8 @@ def main():
         roof = {"kernel": dom, "bound": "hbm", "achieved": amount / dom_t / 1e9, "peak": peaks["hbm"],
                 "unit": "GB/s", "peak_source": "%s copy bandwidth" % peaks["src"]}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(dom, cfg["name"] if cfg["T"] == sy.CONFIGS[cfg["name"]]["T"] else None)
+    roof["algorithmic"] = amount
     gemm_ms = stage_ms["gemm1_swiglu"] + stage_ms["gemm2_down"]
     gemm_tflops = (work["gemm1_swiglu"][1] + work["gemm2_down"][1]) / (gemm_ms / 1e3) / 1e12
 

@@ -5,11 +5,31 @@
 #include "common.cuh"
 #include "internal.h"
 #include "gemm.h"
+#include "sm100.cuh"
 
 namespace moe {
 
 // Device error word written by bounded waits in the kernels (0 = none).
 __device__ int g_device_error = 0;
+
+namespace {
+constexpr int kErrSelfTestTimeout = 0x1ff;
+
+// One thread waits on a fresh mbarrier that nothing ever arrives at, with a clock budget of
+// `budget` cycles; when the budget runs out it records kErrSelfTestTimeout and returns.
+__global__ void selftest_wait_kernel(long long budget) {
+    __shared__ uint64_t bar;
+    __shared__ int never;
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&bar, 1);
+        never = 0;
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !sm100::mbar_wait(&bar, 0, &never, budget))
+        atomicCAS(&g_device_error, 0, kErrSelfTestTimeout);
+}
+}  // namespace
 
 bool config_ok(const moe_config* c) {
     if (!c) return false;
@@ -86,9 +106,17 @@ extern "C" moe_status moe_device_error(int32_t* code) {
     MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
     const int zero = 0;
     MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
-    int32_t tc = 0;
+    int32_t tc = 0, gate = 0;
     MOE_TRY(tc_read_and_clear_error(&tc));
-    *code = v ? v : tc;
+    MOE_TRY(gate_read_and_clear_error(&gate));
+    *code = v ? v : (tc ? tc : gate);
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_selftest_wait_timeout(int64_t budget_cycles, moe_stream_t stream) {
+    if (budget_cycles < 1 || budget_cycles > 4000000000LL) return MOE_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(budget_cycles);
+    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 

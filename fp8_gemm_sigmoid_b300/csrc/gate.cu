@@ -487,6 +487,15 @@ moe_status launch_gate_tc(const moe_config& c, int64_t T, const uint16_t* x, con
 
 size_t gate_scratch_bytes(const moe_config&, int64_t) { return 0; }
 
+moe_status gate_read_and_clear_error(int32_t* code) {
+    int v = 0;
+    MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_gate_error, sizeof(int)));
+    const int zero = 0;
+    MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_gate_error, &zero, sizeof(int)));
+    *code = v;
+    return MOE_OK;
+}
+
 template <typename T>
 static moe_status launch_typed(const moe_config& c, int64_t T_, const T* x, const T* Wg,
                                const float* bias, int32_t* idx, float* w, int32_t* counts,

@@ -34,5 +34,6 @@ moe_status launch_gate(const moe_config& c, int64_t T, const void* x, const void
                        const float* bias, int32_t* idx, float* w, int32_t* counts,
                        float* logits_scratch, cudaStream_t s);
 size_t gate_scratch_bytes(const moe_config& c, int64_t T);
+moe_status gate_read_and_clear_error(int32_t* code);
 
 }  // namespace moe

@@ -57,6 +57,7 @@ _SIGS = {
     "moe_forward": [_cfgp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp,
                     _vp, _vp, _sz, _vp],
     "moe_device_error": [ctypes.POINTER(_i32)],
+    "moe_selftest_wait_timeout": [_i64, _vp],
     "moe_pipeline_workspace_size": [_cfgp, _i64, ctypes.POINTER(_sz)],
     "moe_pipeline_create": [_cfgp, _i64, _vp, _sz, _vp, ctypes.POINTER(_vp)],
     "moe_pipeline_submit": [_vp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp, _vp],
@@ -287,3 +288,7 @@ class MoEPipeline:
             self.close()
         except Exception:
             pass
+
+
+def moe_selftest_wait_timeout(budget_cycles, stream=None):
+    _check("moe_selftest_wait_timeout", _lib_handle().moe_selftest_wait_timeout(int(budget_cycles), _stream(stream)))

@@ -272,6 +272,12 @@ MOE_API moe_status moe_pipeline_destroy(moe_pipeline* pl);
  * it synchronises the device.  *code receives the word; the call then clears it. */
 MOE_API moe_status moe_device_error(int32_t* code);
 
+/* Self-test of the bounded-wait error path (no counterpart on the pages): one thread of a
+ * one-block kernel waits on an mbarrier that nothing arrives at, gives up after
+ * budget_cycles SM clock cycles (1 .. 4e9) and records error word 0x1ff, which the next
+ * moe_device_error returns.  Nothing traps or hangs; the context stays usable. */
+MOE_API moe_status moe_selftest_wait_timeout(int64_t budget_cycles, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
