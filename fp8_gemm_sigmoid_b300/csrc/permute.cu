@@ -6,9 +6,12 @@
 //   1. chunk histogram: counts of each expert inside each chunk of kChunk tokens;
 //   2. scan: offs = exclusive prefix of the counts; base[c][e] = offs[e] + rows of expert e
 //      in chunks before c;
-//   3. positions: inside a chunk, one thread per expert walks the chunk's tokens in order;
-//   4. gather: each destination row copies its token's quantised row; the scales go to a
-//      K-block-major [H/128, R] array, the layout the grouped GEMM reads.
+//   3. positions: inside a chunk, the rank of each (token, slot) among the earlier entries of
+//      its expert, from warp match masks and per-warp counts (one thread per expert walking
+//      the chunk for large top_k * experts);
+//   4. gather: each token's quantised row is read once and written to all of its destination
+//      rows (token-major); the scales go, destination-major, to a K-block-major [H/128, R]
+//      array, the layout the grouped GEMM reads.
 // With a shared expert, group E follows with every token once, in order.
 #include <mutex>
 
@@ -37,46 +40,118 @@ chunk_hist_kernel(int64_t T, int K, int E, const int32_t* __restrict__ idx,
         chunk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One CTA.  Thread e totals expert e's column of chunk counts, an exclusive prefix over the
-// totals gives offs, and a second pass over the column gives each chunk's base.  The rows
-// are derived from topk_idx alone, so every position stays inside [0, T*K).
-__global__ void __launch_bounds__(1024)
+// One CTA of 1024 threads.  Thread (e, part) totals part `part` of expert e's column of
+// chunk counts; the parts' totals give each part's start inside the expert, an exclusive
+// prefix over the experts' totals gives offs, and a second pass over each part writes its
+// chunks' bases.  The rows are derived from topk_idx alone, so every position stays inside
+// [0, T*K).
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
             const int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base,
             int32_t* __restrict__ offs) {
-    __shared__ int32_t part[1024];
-    const int e = threadIdx.x;
+    __shared__ int32_t psum[kScanThreads];  // [part][E]: part totals, then part starts
+    __shared__ int32_t tot[kScanThreads];   // [E]: expert totals, then their inclusive prefix
+    const int tid = threadIdx.x;
+    const int parts = kScanThreads / E;  // E <= 1024
+    const int e = tid % E, part = tid / E;
+    const bool active = part < parts;
+    const int64_t per = (n_chunks + parts - 1) / parts;
+    const int64_t c0 = active ? part * per : 0;
+    const int64_t c1 = active ? (c0 + per < n_chunks ? c0 + per : n_chunks) : 0;
     int32_t v = 0;
-    if (e < E) {
 #pragma unroll 8
-        for (int64_t c = 0; c < n_chunks; ++c) v += chunk_cnt[c * E + e];
-    }
-    part[e] = v;
+    for (int64_t c = c0; c < c1; ++c) v += chunk_cnt[c * E + e];
+    psum[tid] = v;
     __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) {  // inclusive Hillis-Steele scan (E <= 1024)
-        int32_t add = (e >= o) ? part[e - o] : 0;
+    if (tid < E) {
+        int32_t run = 0;
+        for (int q = 0; q < parts; ++q) {
+            const int32_t x = psum[q * E + tid];
+            psum[q * E + tid] = run;
+            run += x;
+        }
+        tot[tid] = run;
+    } else if (tid < kScanThreads) {
+        if (tid >= E) tot[tid] = 0;
+    }
+    __syncthreads();
+    for (int o = 1; o < kScanThreads; o <<= 1) {  // inclusive Hillis-Steele scan over experts
+        const int32_t add = (tid >= o) ? tot[tid - o] : 0;
         __syncthreads();
-        part[e] += add;
+        tot[tid] += add;
         __syncthreads();
     }
-    if (e < E) {
-        const int32_t start = part[e] - v;
-        offs[e] = start;
-        int32_t run = start;
+    if (active) {
+        const int32_t start = (e > 0 ? tot[e - 1] : 0);
+        if (part == 0) offs[e] = start;
+        int32_t run = start + psum[tid];
 #pragma unroll 8
-        for (int64_t c = 0; c < n_chunks; ++c) {
+        for (int64_t c = c0; c < c1; ++c) {
             chunk_base[c * E + e] = run;
             run += chunk_cnt[c * E + e];
         }
     }
-    if (e == 0) {
+    if (tid == 0) {
         const int64_t routed = T * K;
         offs[E] = static_cast<int32_t>(routed);
         if (has_shared) offs[E + 1] = static_cast<int32_t>(routed + T);
     }
 }
 
-// One CTA per chunk; thread e walks the chunk's tokens in order.
+// One CTA per chunk, entries (token, slot) in flat order, 32 per "entry warp".  The rank of an
+// entry among the earlier entries of its expert is its rank inside its entry warp
+// (__match_any_sync) plus the counts of that expert in the earlier entry warps: the stable
+// order, with no atomics.  Shared memory: [n_ewarps][E] counts.
+__global__ void __launch_bounds__(256)
+positions_match_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restrict__ idx,
+                       const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_tok,
+                       int32_t* __restrict__ row_of) {
+    extern __shared__ int32_t wcnt[];  // [n_ew][E]
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int nt = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
+    const int n = nt * K;
+    const int n_ew = (n + 31) / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i = threadIdx.x; i < n_ew * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    for (int ew = warp; ew < n_ew; ew += nwarps) {
+        const int i = ew * 32 + lane;
+        int32_t e = i < n ? idx[t0 * K + i] : -1;
+        if (e < 0 || e >= E) e = -1;  // dropped
+        const uint32_t m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (m & lt) == 0) wcnt[ew * E + e] = __popc(m);  // one leader per expert
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {  // exclusive prefix over entry warps
+        int32_t run = chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+        for (int ew = 0; ew < n_ew; ++ew) {
+            const int32_t x = wcnt[ew * E + e];
+            wcnt[ew * E + e] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    for (int ew = warp; ew < n_ew; ew += nwarps) {
+        const int i = ew * 32 + lane;
+        int32_t e = i < n ? idx[t0 * K + i] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const uint32_t m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) {
+            const int32_t pos = wcnt[ew * E + e] + __popc(m & lt);
+            const int64_t tt = t0 + i / K;
+            perm_tok[pos] = static_cast<int32_t>(tt);
+            row_of[t0 * K + i] = pos;
+        }
+    }
+    if (has_shared)
+        for (int tt = threadIdx.x; tt < nt; tt += blockDim.x)
+            perm_tok[T * K + t0 + tt] = static_cast<int32_t>(t0 + tt);
+}
+
+// Fallback for large K * E (the counts of positions_match_kernel would not fit in shared
+// memory): one CTA per chunk, thread e walks the chunk's entries in order.
 __global__ void __launch_bounds__(256)
 positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restrict__ idx,
                  const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_tok,
@@ -101,42 +176,99 @@ positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restr
             perm_tok[T * K + t0 + tt] = static_cast<int32_t>(t0 + tt);
 }
 
-// Copy destination rows [r0, r0 + 32) from their tokens: the row payloads (row_bytes, a
-// multiple of 16, as 16-byte chunks spread over the block) and, if src_s, the n_scales FP32
-// scales of each row, written K-block-major (dst_s[j * R + r]) so that each warp stores 32
-// consecutive rows of one scale column.
+// Row payloads, token-major: one warp per token reads the token's row (row_bytes, a
+// multiple of 16) once, 8 x 16 bytes per lane at a time, and writes it to each of the token's
+// destination rows: row_of[t, k] for the slots whose expert is in [0, E), and T*K + t for
+// the shared expert.  Reading each token once keeps the source out of DRAM re-reads.
+constexpr int kGatherPiece = 8;  // 16-byte chunks per lane per piece
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(int64_t R, int64_t T, int64_t row_bytes, int n_scales,
-                   const int32_t* __restrict__ perm_tok, const uint8_t* __restrict__ src,
-                   const float* __restrict__ src_s, uint8_t* __restrict__ dst,
-                   float* __restrict__ dst_s) {
-    __shared__ int32_t stok[32];
-    const int chunks = static_cast<int>(row_bytes / 16);
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-    const int64_t n_grp = (R + 31) / 32;
-    for (int64_t gi = blockIdx.x; gi < n_grp; gi += gridDim.x) {
-        const int64_t r0 = gi * 32;
-        const int nr = static_cast<int>(R - r0 < 32 ? R - r0 : 32);
-        __syncthreads();  // the previous group is done with stok
-        if (threadIdx.x < 32) {
-            const int32_t t = threadIdx.x < nr ? perm_tok[r0 + threadIdx.x] : -1;
-            stok[threadIdx.x] = (t >= 0 && t < T) ? t : -1;  // -1: a row no valid (token, slot) claimed
+gather_tokens_kernel(int64_t T, int K, int E, int has_shared, int64_t row_bytes,
+                     const int32_t* __restrict__ idx, const int32_t* __restrict__ row_of,
+                     const uint8_t* __restrict__ src, uint8_t* __restrict__ dst) {
+    const int lane = threadIdx.x % 32;
+    const int64_t chunks = row_bytes / 16;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < T;
+         t += nwarps) {
+        // destination rows of this token (lane k < K holds slot k's row, -1 if dropped)
+        int32_t my_row = -1;
+        if (lane < K) {
+            const int32_t e = idx[t * K + lane];
+            if (e >= 0 && e < E) my_row = row_of[t * K + lane];
         }
-        __syncthreads();
-#pragma unroll 4
-        for (int i = threadIdx.x; i < nr * chunks; i += blockDim.x) {
-            const int rr = i / chunks, ch = i - rr * chunks;
-            const int64_t t = stok[rr];
-            if (t >= 0) d4[(r0 + rr) * chunks + ch] = s4[t * chunks + ch];
-        }
-        if (src_s) {
-            const int lane = threadIdx.x & 31;
-            const int64_t t = lane < nr ? stok[lane] : -1;
-            for (int j = threadIdx.x >> 5; j < n_scales; j += blockDim.x >> 5)
-                if (t >= 0) dst_s[static_cast<int64_t>(j) * R + r0 + lane] = src_s[t * n_scales + j];
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + t * row_bytes);
+        for (int64_t c0 = 0; c0 < chunks; c0 += 32 * kGatherPiece) {
+            uint4 v[kGatherPiece];
+#pragma unroll
+            for (int j = 0; j < kGatherPiece; ++j) {
+                const int64_t c = c0 + j * 32 + lane;
+                if (c < chunks) v[j] = s4[c];
+            }
+            for (int k = 0; k < K + has_shared; ++k) {
+                const int64_t r = k < K ? __shfl_sync(0xffffffffu, my_row, k) : T * K + t;
+                if (r < 0) continue;
+                uint4* d4 = reinterpret_cast<uint4*>(dst + r * row_bytes);
+#pragma unroll
+                for (int j = 0; j < kGatherPiece; ++j) {
+                    const int64_t c = c0 + j * 32 + lane;
+                    if (c < chunks) d4[c] = v[j];
+                }
+            }
         }
     }
+}
+
+// Scales, destination-major: rows [r0, r0 + 32) per step, the n_scales FP32 scales of each
+// row written K-block-major (dst_s[j * R + r]) so that each warp stores 32 consecutive rows
+// of one scale column; the source (src_s [T, n_scales]) is small and read through L2.
+__global__ void __launch_bounds__(256)
+gather_scales_kernel(int64_t R, int64_t T, int n_scales, const int32_t* __restrict__ perm_tok,
+                     const float* __restrict__ src_s, float* __restrict__ dst_s) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n_grp = (R + 31) / 32;
+    for (int64_t gi = blockIdx.x; gi < n_grp; gi += gridDim.x) {
+        const int64_t r = gi * 32 + lane;
+        int64_t t = r < R ? perm_tok[r] : -1;
+        if (t >= T) t = -1;  // a row no valid (token, slot) claimed
+        for (int j = threadIdx.x >> 5; j < n_scales; j += blockDim.x >> 5)
+            if (t >= 0) dst_s[static_cast<int64_t>(j) * R + r] = src_s[t * n_scales + j];
+    }
+}
+
+// The whole permutation on `s`: histogram, scan, positions, row and scale gathers.
+// chunk_cnt / chunk_base: [ceil(T / kChunk), E] int32 scratch each.
+moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_idx, const void* xq,
+                          const float* xs, int32_t* offs, int32_t* perm_tok, int32_t* row_of, void* aq,
+                          float* as, int32_t* chunk_cnt, int32_t* chunk_base, cudaStream_t s) {
+    const int E = c.n_experts, K = c.top_k, S = c.has_shared;
+    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const int64_t n_chunks = ceil_div(T, kChunk);
+    chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(T, K, E, topk_idx,
+                                                                                       chunk_cnt);
+    MOE_LAUNCH_CHECK();
+    scan_kernel<<<1, kScanThreads, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
+    MOE_LAUNCH_CHECK();
+    const size_t match_smem = sizeof(int32_t) * ceil_div(kChunk * K, 32) * E;
+    if (match_smem <= 48 * 1024)
+        positions_match_kernel<<<static_cast<unsigned>(n_chunks), 256, match_smem, s>>>(
+            T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
+    else
+        positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
+            T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
+    MOE_LAUNCH_CHECK();
+    const int64_t R = T * K + T * S;
+    const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
+    const int64_t tok_blocks = ceil_div(T, 8);
+    gather_tokens_kernel<<<static_cast<unsigned>(tok_blocks < 148 * 8 ? tok_blocks : 148 * 8), 256, 0, s>>>(
+        T, K, E, S, row_bytes, topk_idx, row_of, static_cast<const uint8_t*>(xq), static_cast<uint8_t*>(aq));
+    MOE_LAUNCH_CHECK();
+    if (fp8) {
+        const int64_t n_grp = ceil_div(R, 32);
+        gather_scales_kernel<<<static_cast<unsigned>(n_grp < 148 * 8 ? n_grp : 148 * 8), 256, 0, s>>>(
+            R, T, c.hidden / 128, perm_tok, xs, as);
+        MOE_LAUNCH_CHECK();
+    }
+    return MOE_OK;
 }
 
 }  // namespace
@@ -174,23 +306,7 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
         MOE_CUDA_CHECK(cudaMemsetAsync(offs, 0, sizeof(int32_t) * (E + 1 + S), s));
         return MOE_OK;
     }
-    chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
-        T, K, E, topk_idx, chunk_cnt);
-    MOE_LAUNCH_CHECK();
-    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
-    MOE_LAUNCH_CHECK();
-    positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
-        T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
-    MOE_LAUNCH_CHECK();
-    const int64_t R = T * K + T * S;
-    const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
-    const int64_t n_grp = ceil_div(R, 32);
-    const int64_t grid = n_grp < 148 * 8 ? n_grp : 148 * 8;
-    gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
-        fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
-    MOE_LAUNCH_CHECK();
-    return MOE_OK;
+    return launch_permute(c, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as, chunk_cnt, chunk_base, s);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -251,21 +367,5 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T,
     }
     int32_t* chunk_cnt = scratch;
     int32_t* chunk_base = scratch + n_chunks * E;
-    chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(
-        T, K, E, topk_idx, chunk_cnt);
-    MOE_LAUNCH_CHECK();
-    scan_kernel<<<1, 1024, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
-    MOE_LAUNCH_CHECK();
-    positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
-        T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
-    MOE_LAUNCH_CHECK();
-    const int64_t R = T * K + T * S;
-    const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
-    const int64_t n_grp = ceil_div(R, 32);
-    const int64_t grid = n_grp < 148 * 8 ? n_grp : 148 * 8;
-    gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        R, T, row_bytes, fp8 ? c.hidden / 128 : 0, perm_tok, static_cast<const uint8_t*>(xq),
-        fp8 ? xs : nullptr, static_cast<uint8_t*>(aq), fp8 ? as : nullptr);
-    MOE_LAUNCH_CHECK();
-    return MOE_OK;
+    return launch_permute(c, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as, chunk_cnt, chunk_base, s);
 }
