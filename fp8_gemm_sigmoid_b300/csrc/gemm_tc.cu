@@ -9,16 +9,14 @@
 //   P_kb[r, n] = sum_{k in block kb} A[r, k] * W[g, n, k]                (exact FP32 MMA sums)
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles, warp-specialised:
-//   warp 0      producer: lane 0 issues the TMA loads of an A box [128 rows x 128 B] and two
-//               B boxes [128 rows x 128 B] per 128-wide K block into a 3-stage shared-memory
-//               ring (128-byte swizzle); all 32 lanes copy the block's 128 activation scales
-//               and 2 weight scales into a small shared-memory scale ring with asynchronous
-//               copies that complete on the same stage barrier -- the promotion warps then
-//               issue no global loads (a pending global load stalls their tcgen05 fences)
-//               and wait on no extra barrier;
+//   warp 0      TMA producer: A box [128 rows x 128 B] and two B boxes [128 rows x 128 B]
+//               per 128-wide K block into a 3-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates 512 TMEM columns; one lane issues 4 MMAs (K = 32 each) per K block
 //               into one of two 256-column FP32 partial buffers, then commits;
-//   warps 2-3   idle;
+//   warp 2      scale loader: for each K block, the tile's 128 activation scales and its two
+//               weight scales go into a 16-slot shared-memory ring by asynchronous copies, so
+//               that the promotion warps issue no global loads (a pending global load stalls
+//               their tcgen05 fences); warp 3 idles;
 //   warps 4-11  promotion + epilogue: read the partial buffer (tcgen05.ld, 16 columns at a
 //               time with the next load in flight), scale it by as[kb,r] * Ws[g,nb,kb] into
 //               FP32 register pairs (packed FP32x2 FMA), release the buffer; after the last
@@ -50,7 +48,7 @@ constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 384;   // warp 0 TMA + scales, warp 1 MMA + TMEM, 2-3 idle, 4..11 epilogue
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, 2 scales, 3 idle, 4..11 epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
@@ -59,21 +57,20 @@ constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kMaxGroups = 1040;
 constexpr int kOutBox = 32 * 128;                       // one warp's 32 rows x 128 B of output
 constexpr int kOutBytes = kEpiWarps * 2 * kOutBox;      // two staging boxes per epilogue warp
-// Scale ring: when the producer fills the slot of K block k, the promotion has finished block
-// k - 5 (producer waited for the MMA of k - 3, which waited for the release of k - 5), so the
-// slots of k - 4 .. k are the only ones in use: 8 slots never collide.
-constexpr int kScaleSlots = 8;
+constexpr int kScaleSlots = 16;  // K blocks of scale copies in flight (covers L2 latency under load)
 constexpr int kSlotFloats = 132;  // 128 activation scales, 2 weight scales, padding to 16 bytes
 // Control block after the operand ring and the output staging (byte offsets): barriers,
 // TMEM address and flags, amax exchange, warp sums, scale ring, then the tile prefix.
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1;  // full/empty, pfull/pempty, mma_done, ebar
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 2 * kScaleSlots;  // full/empty, pfull/pempty,
+                                                                      // mma_done, ebar, sfull/sempty
 constexpr int kCtlBars = 0, kCtlSlot = (kNumBars * 8 + 15) / 16 * 16, kCtlRed = kCtlSlot + 16,
               kCtlWarpSums = kCtlRed + 2048,
               kCtlScales = kCtlWarpSums + 64, kCtlTiles = kCtlScales + kScaleSlots * kSlotFloats * 4;
 constexpr int kSmemFixed = 1024 + kStages * kStageBytes + kOutBytes + kCtlTiles;
 constexpr int kSmemMax = kSmemFixed + 4 * (kMaxGroups + 1);
 
-enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103 };
+enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103,
+             kErrTimeoutScales = 0x104 };
 
 struct TcParams {
     int n_groups;
@@ -208,7 +205,9 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint64_t* pempty = pfull + 2;           // [2]        epilogue -> MMA
     uint64_t* mma_done = pempty + 2;        // [1]        final MMA drain
     uint64_t* ebar = mma_done + 1;          // [1]        epilogue amax exchange (one phase per tile)
-    static_assert(2 * kStages + 6 <= kNumBars, "barrier block");
+    uint64_t* sfull = ebar + 1;             // [kScaleSlots] scale loaders -> epilogue
+    uint64_t* sempty = sfull + kScaleSlots; // [kScaleSlots] epilogue -> scale loaders
+    static_assert(2 * kStages + 6 + 2 * kScaleSlots <= kNumBars, "barrier block");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + kCtlSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;   // stays 0: drains wait for in-flight work, not for aborts
@@ -220,15 +219,19 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1 + 32);  // expect_tx arrival + 32 lanes' scale copies
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&pfull[b], 2);  // MMA commit + the MMA thread's release arrival
+            mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kEpiWarps);
         }
         mbar_init(mma_done, 1);
         mbar_init(ebar, kEpiThreads);
+        for (int i = 0; i < kScaleSlots; ++i) {
+            mbar_init(&sfull[i], 32);
+            mbar_init(&sempty[i], kEpiWarps);
+        }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -246,56 +249,31 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int total = tile_start[p.n_groups];
 
     if (warp < kEpiWarp0) {
-        // register split: 4 x 48 (producer, MMA, 2 idle) + 8 x 224 (epilogue) <= 12 x 168
+        // register split: 4 x 48 (TMA, MMA, scale loader, idle) + 8 x 224 (epilogue) <= 12 x 168
         asm volatile("setmaxnreg.dec.sync.aligned.u32 48;");
-        if (warp == 0) {
+        if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------------- producer
-            // Lane 0 issues the operand TMA loads of each K block; every lane copies four of
-            // the block's 128 activation scales (lane 0 also the two weight scales) into scale
-            // ring slot kc % kScaleSlots with asynchronous 4-byte copies whose completion
-            // arrives on the same full[s] barrier (32 arrivals + lane 0's expect_tx arrival).
-            // Rows past the group's end and an absent second weight block copy a valid
-            // neighbour: those values are never stored.
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
-            int kc = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileCoord c = decode_tile(p, tile_start, t);
                 const int brow0 = c.g * p.N + b_block(p, c, 0) * 128;
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
-                const int64_t nbk = p.N / 128;
-                const int b1 = b_block(p, c, 1);
-                const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb;
-                const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
-                for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
+                for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
-                    float* slot = sring + (kc % kScaleSlots) * kSlotFloats;
-                    const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = c.row0 + lane + 32 * j;
-                        cp_async4(slot + lane + 32 * j, col + (r < c.row_end ? r : c.row0));
-                    }
-                    if (lane == 0) {
-                        cp_async4(slot + 128, ws0 + kb);
-                        cp_async4(slot + 129, ws1 + kb);
-                    }
-                    cp_async_mbar_arrive(&full[s]);
-                    if (lane == 0) {
-                        uint8_t* sa = smem + s * kStageBytes;
-                        uint8_t* sb = sa + kABytes;
-                        mbar_arrive_expect_tx(&full[s], kStageBytes);
-                        tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
-                        tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
-                        tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
-                    }
+                    uint8_t* sa = smem + s * kStageBytes;
+                    uint8_t* sb = sa + kABytes;
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
+                    tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
+                    tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
                     ++issued;
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok && lane == 0) {
+            if (!ok) {
                 *abort_flag = 1;
                 atomicCAS(&g_tc_error, 0, kErrTimeoutProducer);
             }
@@ -304,7 +282,6 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (--s < 0) { s = kStages - 1; ph ^= 1u; }
                 mbar_wait(&full[s], ph, never, kWaitBudget);
             }
-            cp_async_wait_all();
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
@@ -327,10 +304,6 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                    idesc, k > 0 ? 1u : 0u);
                     mma_commit(&empty[s]);
                     mma_commit(&pfull[b]);
-                    // second arrival on pfull: a release by this thread, which acquired full[s]
-                    // (and with it the block's scale copies) -- the promotion warps read the
-                    // scale slot after pfull completes
-                    mbar_arrive(&pfull[b]);
                     pbits ^= 1u << b;
                     b ^= 1;
                     if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -343,6 +316,46 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             // drain: every MMA this thread issued has completed once mma_done flips
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, never, kWaitBudget);
+        } else if (warp == 2) {
+            // ---------------------------------------------------------------- scale loader
+            // For each K block, once the ring slot is free: every lane copies four activation
+            // scales and lane 0 the two weight scales with asynchronous 4-byte global->shared
+            // copies, then each lane's copies arrive on the slot's barrier when they land
+            // (cp.async.mbarrier.arrive.noinc; 32 arrivals complete the phase).  Up to
+            // kScaleSlots blocks of copies are in flight.  Rows past the group's end and the
+            // absent second weight block copy a valid neighbour: those values are never stored.
+            uint32_t sph = 0;  // bit i: parity of the next use of slot i
+            bool ok = true;
+            int kc = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile(p, tile_start, t);
+                const int64_t nbk = p.N / 128;
+                const int b1 = b_block(p, c, 1);
+                const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb;
+                const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
+                for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
+                    const int i = kc % kScaleSlots;
+                    if (!mbar_wait(&sempty[i], ((sph >> i) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                    sph ^= 1u << i;
+                    float* slot = sring + i * kSlotFloats;
+                    const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = c.row0 + lane + 32 * j;
+                        cp_async4(slot + lane + 32 * j, col + (r < c.row_end ? r : c.row0));
+                    }
+                    if (lane == 0) {
+                        cp_async4(slot + 128, ws0 + kb);
+                        cp_async4(slot + 129, ws1 + kb);
+                    }
+                    cp_async_mbar_arrive(&sfull[i]);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicCAS(&g_tc_error, 0, kErrTimeoutScales);
+            }
+            cp_async_wait_all();  // nothing in flight when the CTA exits
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
@@ -357,6 +370,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int b = 0;
         uint32_t pbits = 0;  // bit b: parity of the next phase of pfull[b]
         uint32_t eph = 0;    // phase of ebar
+        uint32_t sfp = 0;    // bit i: parity of the next phase of sfull[i]
         int kc = 0;          // K blocks promoted so far (scale ring position)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -370,12 +384,17 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
             for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
-                if (!mbar_wait(&pfull[b], (pbits >> b) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                 // this block's scales from the ring: as[kb, row] * Ws[g, half, kb]
-                const float* slot = sring + (kc % kScaleSlots) * kSlotFloats;
+                const int si = kc % kScaleSlots;
+                if (!mbar_wait(&sfull[si], (sfp >> si) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                sfp ^= 1u << si;
+                const float* slot = sring + si * kSlotFloats;
                 const float sa = slot[trow];
                 const float sc0 = sa * slot[128], sc1 = sa * slot[129];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[si]);
                 const float2 s0 = make_float2(sc0, sc0), s1 = make_float2(sc1, sc1);
+                if (!mbar_wait(&pfull[b], (pbits >> b) & 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(b * kBN);
