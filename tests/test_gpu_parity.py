@@ -432,8 +432,8 @@ def test_layer_fp8_zero_tokens(moe, sy, orc):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,n_sample", [("v3_decode", 24), ("v3_prefill", 8), ("v3_skewed", 8),
-                                           ("v3_top1", 16)])
+@pytest.mark.parametrize("name,n_sample", [("v3_decode", 64), ("v3_prefill", 32), ("v3_skewed", 32),
+                                           ("v3_top1", 48)])
 def test_layer_v3_full_size(moe, sy, orc, v3, name, n_sample):
     cfg = sy.config(name)
     r = _check_layer(moe, sy, orc, cfg, n_sample=n_sample, v3=v3)
