@@ -349,9 +349,6 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         bool ok = mbar_wait(acc_full, 0, abort_flag, kGtWaitBudget);
         ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
         tc_fence_after();
-        // x has been streamed: a programmatic dependent (the activation quantiser, which reads
-        // only x) may start and overlap the selection below
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicCAS(&g_gate_error, 0, 0x203);

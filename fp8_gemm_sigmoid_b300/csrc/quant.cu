@@ -55,10 +55,6 @@ quant_1x128_kernel(int64_t n_tiles, const uint4* __restrict__ x, uint2* __restri
             if (sub == 0) s[tile] = scale;
         }
     }
-    // Launched as a programmatic dependent of the gate (it reads only x, so it may overlap the
-    // gate's selection tail); it completes only after the kernel before it has, so that the
-    // next kernel in the stream is ordered after both.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // One CTA per 128x128 block: amax over the block, then encode.  w is [n, rows, cols].
@@ -119,20 +115,9 @@ extern "C" moe_status moe_quant_1x128(int64_t rows, int64_t cols, const uint16_t
     const int64_t tiles = rows * (cols / 128);
     const int64_t blocks = ceil_div(tiles, 16);  // 16 tiles per 256-thread CTA
     const unsigned grid = static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
-    // programmatic dependent launch: may start once the previous kernel signals (the gate does
-    // after its logit MMAs); a kernel that does not signal is simply waited for
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(grid);
-    lc.blockDim = dim3(256);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, quant_1x128_kernel, tiles, reinterpret_cast<const uint4*>(x),
-                                      reinterpret_cast<uint2*>(q), s));
+    quant_1x128_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        tiles, reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), s);
+    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
