@@ -277,6 +277,17 @@ def cpu_baseline(cfg, layer, n_tok):
     return dt, oracle.num_threads()
 
 
+def metric_name(cfg):
+    return "MoE layer tokens/s and grouped-GEMM TFLOPS (%% of FP8 peak) at T=%d, 1 B300" % cfg["T"]
+
+
+def config_dict(cfg, world):
+    return {"workload": cfg["name"], "T": cfg["T"], "hidden": cfg["hidden"], "inter": cfg["inter"],
+            "n_experts": cfg["n_experts"], "top_k": cfg["top_k"], "shared": cfg["has_shared"],
+            "l2": "inputs larger than L2 (11.3 GB of FP8 expert weights per step)",
+            "parallelism": "replicas x%d" % world}
+
+
 def run_reference(args, cfg, rank, world):
     """The reference arm: the CPU oracle timed on the host cores, rank 0 only."""
     if rank != 0:
@@ -294,11 +305,11 @@ def run_reference(args, cfg, rank, world):
     tot = sum(times)
     val = n * args.steps / tot
     line = {
-        "impl": "reference", "metric": "MoE layer tokens/s (CPU oracle)", "value": val,
+        "impl": "reference", "metric": metric_name(cfg), "value": val,
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg["name"], "T": cfg["T"], "sample_tokens": n},
+        "config": config_dict(cfg, 1),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": "first %d tokens of the %s batch as a layer of their own, per step" % (n, cfg["name"])},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -462,7 +473,7 @@ def main():
                          "expert FFNs, combine; weights quantised beforehand)" % (n, T)}
 
     line = {
-        "metric": "MoE layer tokens/s and grouped-GEMM TFLOPS (%% of FP8 peak) at T=%d, 1 B300" % T,
+        "metric": metric_name(cfg),
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
@@ -474,10 +485,7 @@ def main():
         "vs_baseline": None,
         "dtype": "fp8-e4m3 (FP32 accumulation), bf16 activations",
         "data": "synthetic",
-        "config": {"workload": cfg["name"], "T": T, "hidden": cfg["hidden"], "inter": cfg["inter"],
-                   "n_experts": cfg["n_experts"], "top_k": cfg["top_k"], "shared": cfg["has_shared"],
-                   "l2": "inputs larger than L2 (11.3 GB of FP8 expert weights per step)",
-                   "parallelism": "replicas x%d" % world},
+        "config": config_dict(cfg, world),
         "grouped_gemm": {"ms": gemm_ms, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
         "stages": stages,
         "roofline": roof,
