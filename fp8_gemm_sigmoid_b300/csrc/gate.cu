@@ -242,6 +242,13 @@ struct GateTcParams {
 // sigmoid with the fast exponential and division intrinsics (a few ulp in FP32; the selection
 // is compared with the exact scores only where its margin exceeds 1e-5, and the weights within
 // 2e-5 of the routing scale).  x -> -inf gives 0, x -> +inf gives 1.
+// An unsigned key whose order is the order of the floats (negative values bit-inverted,
+// positive ones with the sign bit set); 0 is below every float's key except -NaN patterns.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __global__ void __launch_bounds__(kGtThreads, 1)
@@ -378,15 +385,12 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             gsc[tl * kGtMaxG + g] = a1 + a2;
         }
         __syncthreads();
-        // pass 2, one warp per token (warp w takes tokens w, w + 16, ...): lane l holds experts
-        // l + 32 j; keep topk_group groups by the group scores, then top_k rounds of a
-        // warp arg-max over the kept experts' selection scores (ties to the lower index, slots
-        // in descending score).  The un-biased scores are recomputed from the stored logits
-        // with the same instructions as in pass 1.
+        // kept groups (topk_group by group score, ties to the lower index) and the slots they
+        // cover, once per token: slot j of a lane holds expert lane + 32 j, in group j / cpg
+        uint32_t* kmask = reinterpret_cast<uint32_t*>(lg + kGtM * lgs);  // [kGtM]
         const int epl = p.E / 32;
-        for (int tok = warp; tok < kGtM && ok; tok += kGtThreads / 32) {
-            const int64_t tt = t0 + tok;
-            if (tt >= p.T) break;
+        if (threadIdx.x < kGtM) {
+            const int tok = threadIdx.x;
             uint32_t kept = 0;
             for (int r = 0; r < p.TG; ++r) {
                 int best = -1;
@@ -397,9 +401,23 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 }
                 kept |= 1u << (best < 0 ? 0 : best);
             }
-            uint32_t skept = 0;  // bit j: slot j (group j / cpg) is in a kept group
+            uint32_t skept = 0;
             for (int j = 0; j < epl; ++j)
                 if ((kept >> (j / cpg)) & 1u) skept |= 1u << j;
+            kmask[tok] = skept;
+        }
+        __syncthreads();
+        // pass 2, one warp per token (warp w takes tokens w, w + 16, ...): top_k rounds of a warp
+        // arg-max over the kept experts' selection scores, ties to the lower expert index, slots
+        // in descending score.  Each round: the lane-local best (slots in ascending index, so a
+        // strict '>' keeps the lowest index among equals), the warp maximum of an
+        // order-preserving integer key of the score, then the warp minimum of the index among
+        // the lanes holding that maximum.  The un-biased scores are recomputed from the stored
+        // logits with the same instructions as in pass 1.
+        for (int tok = warp; tok < kGtM && ok; tok += kGtThreads / 32) {
+            const int64_t tt = t0 + tok;
+            if (tt >= p.T) break;
+            const uint32_t skept = kmask[tok];
             float sv[kGtMaxE / 32], cv[kGtMaxE / 32];
 #pragma unroll
             for (int j = 0; j < kGtMaxE / 32; ++j) {
@@ -411,28 +429,21 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     cv[j] = sv[j] + sbias[e];
                 }
             }
-            uint32_t taken = 0;
+            uint32_t avail = skept;  // kept slots not yet chosen
             float den = 0.f, my_w = 0.f;
             int my_e = 0;
             for (int k = 0; k < p.K; ++k) {
                 float v = -INFINITY, s_best = 0.f;
-                int i = 0x7fffffff;
+                int jb = -1;
 #pragma unroll
-                for (int j = 0; j < kGtMaxE / 32; ++j) {
-                    const int e = lane + 32 * j;
-                    if (((skept & ~taken) >> j) & 1u && (cv[j] > v || (cv[j] == v && e < i))) {
-                        v = cv[j]; i = e; s_best = sv[j];
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-                    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
-                }
+                for (int j = 0; j < kGtMaxE / 32; ++j)
+                    if (((avail >> j) & 1u) && (jb < 0 || cv[j] > v)) { v = cv[j]; jb = j; s_best = sv[j]; }
+                const uint32_t key = jb < 0 ? 0u : order_key(v + 0.0f);  // (-0 + 0 = +0: equal zeros, equal keys)
+                const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+                int i = __reduce_min_sync(0xffffffffu, (jb >= 0 && key == kmax) ? lane + 32 * jb : 0x7fffffff);
                 if (i >= p.E) i = 0;  // no candidate (NaN scores): expert 0, never out of range
                 const int owner = i & 31;
-                if (lane == owner) taken |= 1u << (i >> 5);
+                if (lane == owner) avail &= ~(1u << (i >> 5));
                 const float sw = __shfl_sync(0xffffffffu, s_best, owner);
                 den = den + sw;
                 if (lane == k) { my_w = sw; my_e = i; }
