@@ -136,6 +136,7 @@ extern "C" moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs
                                            size_t ws_bytes, moe_stream_t stream) {
     if (n_groups < 1 || rows < 0 || N <= 0 || Kdim <= 0 || N % 128 || Kdim % 128)
         return MOE_ERR_INVALID_ARG;
+    if (n_groups > kMaxGemmGroups) return MOE_ERR_UNSUPPORTED;  // the tile schedule lives in shared memory
     if (epilogue == MOE_EPI_SWIGLU_QUANT) {
         if (N % 256 != 0 || !out_s || !aligned16(out_s)) return MOE_ERR_INVALID_ARG;
     } else if (epilogue != MOE_EPI_STORE) {

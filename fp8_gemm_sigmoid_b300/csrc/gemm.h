@@ -26,6 +26,7 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
                                       const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
                                       cudaStream_t s);
 size_t tc_scratch_bytes(int32_t n_groups);
+constexpr int32_t kMaxGemmGroups = 1040;  // groups of one grouped-GEMM call (tile schedule in shared memory)
 moe_status tc_read_and_clear_error(int32_t* code);
 // 2D TMA map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements, box
 // [box_rows x box_cols elements] (box_cols * elem_bytes == 128), 128-byte swizzle.

@@ -54,7 +54,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
-constexpr int kMaxGroups = 1040;
+constexpr int kMaxGroups = kMaxGemmGroups;
 constexpr int kOutBox = 32 * 128;                       // one warp's 32 rows x 128 B of output
 constexpr int kOutBytes = kEpiWarps * 2 * kOutBox;      // two staging boxes per epilogue warp
 constexpr int kScaleSlots = 16;  // K blocks of scale copies in flight (covers L2 latency under load)
@@ -575,7 +575,6 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     const bool swiglu = (epilogue == MOE_EPI_SWIGLU_QUANT);
     if (N % 128 != 0 || (swiglu && N % 256 != 0)) return MOE_ERR_INVALID_ARG;
     if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
-    if (n_groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
     CUtensorMap tmA, tmB, tmO;
     if (!make_map_u8(&tmA, A, rows, Kd)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tmB, W, static_cast<int64_t>(n_groups) * N, Kd)) return MOE_ERR_CUDA;

@@ -78,6 +78,9 @@ def test_host_side_argument_checks(moe):
                                   vp(16), vp(16), vp(16), 0, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_grouped_gemm_fp8(2, vp(16), 10, 256, 256, vp(16), vp(16), vp(16), vp(16), 0,
                                   vp(16), vp(17), vp(16), 0, None) == moe.MOE_ERR_INVALID_ARG
+    # more groups than the in-kernel tile schedule holds
+    assert L.moe_grouped_gemm_fp8(1041, vp(16), 10, 256, 256, vp(16), vp(16), vp(16), vp(16), 0,
+                                  vp(16), vp(16), vp(16), 0, None) == moe.MOE_ERR_UNSUPPORTED
     from fp8_gemm_sigmoid_b300 import synthetic as sy
     cfg = moe.make_config(sy.config("v3_prefill"))
     need = ctypes.c_size_t(0)
