@@ -185,7 +185,7 @@ def _random_groups(rng, E, total, empty=()):
     return c
 
 
-@pytest.mark.parametrize("H,I,E,R", [(384, 256, 5, 700), (7168, 2048, 4, 300)])
+@pytest.mark.parametrize("H,I,E,R", [(384, 256, 5, 700), (640, 384, 3, 400), (7168, 2048, 4, 300)])
 def test_grouped_gemm_fp8_swiglu_and_down(moe, orc, H, I, E, R):
     rng = np.random.default_rng(H + R)
     counts = _random_groups(rng, E, R, empty=(1,))
