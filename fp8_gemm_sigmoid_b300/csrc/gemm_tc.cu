@@ -86,11 +86,17 @@ struct TcParams {
     float* out_s;               // SwiGLU: [N/256, rows] (K-block-major, as the next GEMM reads it)
 };
 
+constexpr int kNFastMTiles = 32;  // m-tiles (4096 rows) above which a group runs n-fastest
+
 struct TileCoord {
     int g, m_local, n_tile;
     int row0, row_end;
 };
 
+// Tile t of the schedule.  In a group of up to kNFastMTiles m-tiles the m-tiles run fastest:
+// the concurrent tiles share each weight tile in L2.  A larger group (the shared expert's T
+// rows) runs its n-tiles fastest instead, so that its A rows, which would not stay in L2
+// between n-tiles, are read once while its weight tiles stay in L2.
 __device__ __forceinline__ TileCoord decode_tile(const TcParams& p, const int32_t* tile_start, int t) {
     TileCoord c;
     c.g = find_group(tile_start, p.n_groups, t);
@@ -98,8 +104,13 @@ __device__ __forceinline__ TileCoord decode_tile(const TcParams& p, const int32_
     c.row0 = p.offs[c.g];
     c.row_end = p.offs[c.g + 1];
     const int mt = (c.row_end - c.row0 + kBM - 1) / kBM;
-    c.n_tile = local / mt;
-    c.m_local = local - c.n_tile * mt;
+    if (mt > kNFastMTiles) {  // a large group: its n-tiles run fastest, each A tile is read once
+        c.m_local = local / p.n_tiles_n;
+        c.n_tile = local - c.m_local * p.n_tiles_n;
+    } else {
+        c.n_tile = local / mt;
+        c.m_local = local - c.n_tile * mt;
+    }
     c.row0 += c.m_local * kBM;
     return c;
 }
