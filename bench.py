@@ -32,9 +32,11 @@ KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gat
                   "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu"}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
-# kernels each entry point launches (memsets excluded); summed into gpu_launches
-LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_permute": 4,
-            "moe_grouped_gemm_fp8/swiglu": 3, "moe_grouped_gemm_fp8/store": 2,
+# kernels each entry point launches in the FP8 layer (memsets excluded); summed into
+# gpu_launches.  moe_permute: chunk histogram, scan, positions, row gather, scale gather.
+# Each grouped GEMM is one persistent kernel (its tile schedule is built in shared memory).
+LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_permute": 5,
+            "moe_grouped_gemm_fp8/swiglu": 1, "moe_grouped_gemm_fp8/store": 1,
             "moe_combine": 1, "moe_bias_update": 1}
 
 

@@ -40,62 +40,82 @@ chunk_hist_kernel(int64_t T, int K, int E, const int32_t* __restrict__ idx,
         chunk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One CTA of 1024 threads.  Thread (e, part) totals part `part` of expert e's column of
-// chunk counts; the parts' totals give each part's start inside the expert, an exclusive
-// prefix over the experts' totals gives offs, and a second pass over each part writes its
-// chunks' bases.  The rows are derived from topk_idx alone, so every position stays inside
-// [0, T*K).
+// One CTA per 32 experts (E <= 1024), 1024 threads.  Every CTA totals every expert over all
+// chunks (coalesced, independent loads of the [n_chunks, E] counts) and takes the exclusive
+// prefix of the totals, the start of each expert's rows; CTA 0 writes it to offs.  Each CTA
+// then writes the chunk bases of its own 32 experts: warp w sums part w of the chunks of
+// expert (32 * blockIdx.x + lane), and the parts before it give the part's start.  The rows
+// are derived from topk_idx alone, so every position stays inside [0, T*K).
 constexpr int kScanThreads = 1024;
+constexpr int kScanSlice = 32;  // experts per CTA in the base pass (one per lane)
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
             const int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base,
             int32_t* __restrict__ offs) {
-    __shared__ int32_t psum[kScanThreads];  // [part][E]: part totals, then part starts
-    __shared__ int32_t tot[kScanThreads];   // [E]: expert totals, then their inclusive prefix
-    const int tid = threadIdx.x;
-    const int parts = kScanThreads / E;  // E <= 1024
-    const int e = tid % E, part = tid / E;
-    const bool active = part < parts;
-    const int64_t per = (n_chunks + parts - 1) / parts;
-    const int64_t c0 = active ? part * per : 0;
-    const int64_t c1 = active ? (c0 + per < n_chunks ? c0 + per : n_chunks) : 0;
-    int32_t v = 0;
-#pragma unroll 8
-    for (int64_t c = c0; c < c1; ++c) v += chunk_cnt[c * E + e];
-    psum[tid] = v;
+    __shared__ int32_t tot[kScanThreads];                  // expert totals, then their starts
+    __shared__ int32_t wsum[kScanThreads / 32];
+    __shared__ int32_t psum[kScanThreads / 32][kScanSlice + 1];  // [part][expert of the slice]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    tot[tid] = 0;
     __syncthreads();
-    if (tid < E) {
-        int32_t run = 0;
-        for (int q = 0; q < parts; ++q) {
-            const int32_t x = psum[q * E + tid];
-            psum[q * E + tid] = run;
-            run += x;
+    const int64_t n = n_chunks * E;
+    if (kScanThreads % E == 0) {  // every count a thread reads belongs to expert tid % E
+        int32_t v = 0;
+#pragma unroll 8
+        for (int64_t i = tid; i < n; i += kScanThreads) v += chunk_cnt[i];
+        atomicAdd(&tot[tid % E], v);
+    } else {
+        for (int64_t i = tid; i < n; i += kScanThreads) atomicAdd(&tot[i % E], chunk_cnt[i]);
+    }
+    __syncthreads();
+    // exclusive prefix over the experts (entries past E are 0): warp scans, then warp totals
+    const int32_t x = tot[tid];
+    int32_t incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t own = wsum[lane];
+        int32_t w = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
         }
-        tot[tid] = run;
-    } else if (tid < kScanThreads) {
-        if (tid >= E) tot[tid] = 0;
+        wsum[lane] = w - own;
     }
     __syncthreads();
-    for (int o = 1; o < kScanThreads; o <<= 1) {  // inclusive Hillis-Steele scan over experts
-        const int32_t add = (tid >= o) ? tot[tid - o] : 0;
-        __syncthreads();
-        tot[tid] += add;
-        __syncthreads();
+    tot[tid] = wsum[warp] + incl - x;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        if (tid < E) offs[tid] = tot[tid];
+        if (tid == 0) {
+            const int64_t routed = T * K;
+            offs[E] = static_cast<int32_t>(routed);
+            if (has_shared) offs[E + 1] = static_cast<int32_t>(routed + T);
+        }
     }
-    if (active) {
-        const int32_t start = (e > 0 ? tot[e - 1] : 0);
-        if (part == 0) offs[e] = start;
-        int32_t run = start + psum[tid];
+    const int e = blockIdx.x * kScanSlice + lane;
+    const int64_t per = (n_chunks + kScanThreads / 32 - 1) / (kScanThreads / 32);
+    const int64_t c0 = min(static_cast<int64_t>(warp) * per, n_chunks), c1 = min(c0 + per, n_chunks);
+    int32_t v = 0;
+    if (e < E) {
 #pragma unroll 8
+        for (int64_t c = c0; c < c1; ++c) v += chunk_cnt[c * E + e];
+    }
+    psum[warp][lane] = v;
+    __syncthreads();
+    if (e < E) {
+        int32_t run = tot[e];
+        for (int q = 0; q < warp; ++q) run += psum[q][lane];
         for (int64_t c = c0; c < c1; ++c) {
             chunk_base[c * E + e] = run;
             run += chunk_cnt[c * E + e];
         }
-    }
-    if (tid == 0) {
-        const int64_t routed = T * K;
-        offs[E] = static_cast<int32_t>(routed);
-        if (has_shared) offs[E + 1] = static_cast<int32_t>(routed + T);
     }
 }
 
@@ -218,20 +238,36 @@ gather_tokens_kernel(int64_t T, int K, int E, int has_shared, int64_t row_bytes,
     }
 }
 
-// Scales, destination-major: rows [r0, r0 + 32) per step, the n_scales FP32 scales of each
-// row written K-block-major (dst_s[j * R + r]) so that each warp stores 32 consecutive rows
-// of one scale column; the source (src_s [T, n_scales]) is small and read through L2.
-__global__ void __launch_bounds__(256)
+// Scales, destination-major: one warp per 32 consecutive destination rows.  For each tile of
+// 32 scale columns the warp reads, row by row, the row's run of scales from its token (one
+// coalesced load of up to 128 bytes per row), transposes the 32 x 32 tile through shared
+// memory, and writes each column's 32 rows as one coalesced store to the K-block-major
+// dst_s[j * R + r].  Rows no valid (token, slot) claimed are not written.
+constexpr int kScaleWarps = 8;
+__global__ void __launch_bounds__(kScaleWarps * 32)
 gather_scales_kernel(int64_t R, int64_t T, int n_scales, const int32_t* __restrict__ perm_tok,
                      const float* __restrict__ src_s, float* __restrict__ dst_s) {
-    const int lane = threadIdx.x & 31;
+    __shared__ float tile[kScaleWarps][32][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float (*sm)[33] = tile[w];
     const int64_t n_grp = (R + 31) / 32;
-    for (int64_t gi = blockIdx.x; gi < n_grp; gi += gridDim.x) {
+    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * kScaleWarps + w; gi < n_grp;
+         gi += static_cast<int64_t>(gridDim.x) * kScaleWarps) {
         const int64_t r = gi * 32 + lane;
         int64_t t = r < R ? perm_tok[r] : -1;
-        if (t >= T) t = -1;  // a row no valid (token, slot) claimed
-        for (int j = threadIdx.x >> 5; j < n_scales; j += blockDim.x >> 5)
-            if (t >= 0) dst_s[static_cast<int64_t>(j) * R + r] = src_s[t * n_scales + j];
+        if (t >= T) t = -1;
+        for (int j0 = 0; j0 < n_scales; j0 += 32) {
+            const int j = j0 + lane;
+            for (int i = 0; i < 32; ++i) {  // row i of the group: its token's scales j0 .. j0 + 31
+                const int64_t ti = __shfl_sync(0xffffffffu, t, i);
+                sm[lane][i] = (ti >= 0 && j < n_scales) ? src_s[ti * n_scales + j] : 0.f;
+            }
+            __syncwarp();
+            const int nj = min(32, n_scales - j0);
+            if (t >= 0)
+                for (int jj = 0; jj < nj; ++jj) dst_s[static_cast<int64_t>(j0 + jj) * R + r] = sm[jj][lane];
+            __syncwarp();
+        }
     }
 }
 
@@ -246,7 +282,8 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
     chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(T, K, E, topk_idx,
                                                                                        chunk_cnt);
     MOE_LAUNCH_CHECK();
-    scan_kernel<<<1, kScanThreads, 0, s>>>(T, K, E, S, n_chunks, chunk_cnt, chunk_base, offs);
+    scan_kernel<<<static_cast<unsigned>(ceil_div(E, kScanSlice)), kScanThreads, 0, s>>>(T, K, E, S, n_chunks,
+                                                                                      chunk_cnt, chunk_base, offs);
     MOE_LAUNCH_CHECK();
     const size_t match_smem = sizeof(int32_t) * ceil_div(kChunk * K, 32) * E;
     if (match_smem <= 48 * 1024)
@@ -263,8 +300,8 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
         T, K, E, S, row_bytes, topk_idx, row_of, static_cast<const uint8_t*>(xq), static_cast<uint8_t*>(aq));
     MOE_LAUNCH_CHECK();
     if (fp8) {
-        const int64_t n_grp = ceil_div(R, 32);
-        gather_scales_kernel<<<static_cast<unsigned>(n_grp < 148 * 8 ? n_grp : 148 * 8), 256, 0, s>>>(
+        const int64_t blocks = ceil_div(ceil_div(R, 32), kScaleWarps);
+        gather_scales_kernel<<<static_cast<unsigned>(blocks < 148 * 8 ? blocks : 148 * 8), kScaleWarps * 32, 0, s>>>(
             R, T, c.hidden / 128, perm_tok, xs, as);
         MOE_LAUNCH_CHECK();
     }
