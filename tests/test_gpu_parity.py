@@ -141,8 +141,12 @@ def test_gate_ties_and_forced_experts(moe, orc):
 
 # ------------------------------------------------------------------ permutation
 
+# (500, 96, 6, 1): an expert count that does not divide the scan's 1024 threads;
+# (300, 1024, 32, 1): top_k * experts too large for the match kernel's shared-memory counts,
+# so the positions come from the one-thread-per-expert fallback.
 @pytest.mark.parametrize("T,E,K,S", [(1, 16, 2, 1), (300, 256, 8, 1), (4097, 256, 8, 0),
-                                     (129, 16, 2, 1), (1000, 256, 1, 1)])
+                                     (129, 16, 2, 1), (1000, 256, 1, 1), (500, 96, 6, 1),
+                                     (300, 1024, 32, 1)])
 def test_permute_bitexact(moe, orc, T, E, K, S):
     rng = np.random.default_rng(T + E + K)
     # skewed synthetic routing: some experts empty, one hot expert
@@ -150,9 +154,9 @@ def test_permute_bitexact(moe, orc, T, E, K, S):
     p[3] += 2.0
     p /= p.sum()
     idx = np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(T)]).astype(np.int32)
-    cfg = dict(hidden=256, inter=128, n_experts=E, n_group=8 if E == 256 else 4,
-               topk_group=4 if E == 256 else 2, top_k=K, routed_scaling_factor=1.0,
-               has_shared=S, mode="fp8")
+    G, TG = {256: (8, 4), 1024: (32, 32)}.get(E, (4, 2))
+    cfg = dict(hidden=256, inter=128, n_experts=E, n_group=G, topk_group=TG, top_k=K,
+               routed_scaling_factor=1.0, has_shared=S, mode="fp8")
     H = cfg["hidden"]
     g = torch.Generator(device=DEV).manual_seed(T)
     xq = torch.randint(0, 255, (T, H), generator=g, device=DEV, dtype=torch.uint8)
