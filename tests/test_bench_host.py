@@ -1,0 +1,58 @@
+"""Host-side logic of bench.py that decides reported numbers: the algorithmic work behind every
+roofline fraction, and the gating of recorded DRAM traffic on the kernel source it was
+measured on.  CPU only."""
+import hashlib
+import os
+
+import bench
+from fp8_gemm_sigmoid_b300 import synthetic as sy
+
+
+def test_stage_work_matches_the_layer_closed_forms():
+    # Prefill shape: per token, 8 routed rows and the shared expert's row go through
+    # [gate; up] (2*H*2I flops each) and down (2*I*H flops each).
+    cfg = sy.config("v3_prefill")
+    T, H, I, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["top_k"]
+    w = bench.stage_work(cfg)
+    per_token = (w["gemm1_swiglu"][1] + w["gemm2_down"][1]) / T
+    assert per_token == (K + 1) * (2 * H * 2 * I + 2 * I * H)
+    assert abs(per_token / 1e6 - 792.7) < 0.05  # 792.7 MFLOP per token at H=7168, I=2048
+    assert w["gemm1_swiglu"][0] == w["gemm2_down"][0] == "tensor"
+    # the gate reads x (BF16) and Wg once; the combine reads 9 BF16 rows and writes y per token
+    assert w["gate"][1] >= T * H * 2 and w["gate"][1] < T * H * 2 * 1.05
+    assert w["combine"][1] >= (K + 1) * T * H * 2 + T * H * 2
+    for k in ("gate", "quant", "permute", "combine"):
+        assert w[k][0] == "hbm"
+    # no shared expert: one row per routed slot only
+    cfg0 = dict(cfg, has_shared=0)
+    assert bench.stage_work(cfg0)["gemm2_down"][1] == T * K * 2 * I * H
+
+
+def _sha(stage):
+    path = os.path.join(bench.ROOT, "fp8_gemm_sigmoid_b300", "csrc", bench.KERNEL_SOURCES[stage])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def test_measured_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.txt"
+    f.write_text("# workload stage sha read write\n"
+                 "v3_prefill gate %s 1000 24\n"
+                 "v3_prefill combine %s 7 8\n" % (_sha("gate"), "0" * 64))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic("gate", "v3_prefill") == 1024
+    assert bench.measured_traffic("combine", "v3_prefill") is None  # source changed since
+    assert bench.measured_traffic("gate", "v3_decode") is None       # other workload
+    assert bench.measured_traffic("bias_update", "v3_prefill") is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
+    assert bench.measured_traffic("gate", "v3_prefill") is None
+
+
+def test_recorded_traffic_file_is_well_formed():
+    with open(bench.TRAFFIC_FILE) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for workload, stage, sha, rd, wr in rows:
+        assert workload in sy.CONFIGS and stage in bench.KERNEL_SOURCES
+        assert len(sha) == 64 and int(sha, 16) >= 0
+        assert int(rd) > 0 and int(wr) >= 0
