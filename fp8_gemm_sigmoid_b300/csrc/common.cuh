@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/moe.h"
 
 #define MOE_CUDA_CHECK(expr)                                                    \
@@ -27,6 +29,31 @@
 namespace moe {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side set-up that must run once on each device a process uses (kernel attributes such
+// as the dynamic shared-memory limit are per device).  Each call site owns one instance.
+struct PerDeviceOnce {
+    static constexpr int kMaxDevices = 64;
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    cudaError_t err[kMaxDevices] = {};
+};
+
+// Runs f() on the current device the first time this call site sees that device, and returns
+// its result then and on every later call there.
+template <typename F>
+cudaError_t once_per_device(PerDeviceOnce& o, F&& f) {
+    int dev = -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= PerDeviceOnce::kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(o.mu);
+    if (!o.done[dev]) {
+        o.err[dev] = f();
+        o.done[dev] = true;
+    }
+    return o.err[dev];
+}
 
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

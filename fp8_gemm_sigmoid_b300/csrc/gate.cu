@@ -481,12 +481,10 @@ moe_status launch_gate_tc(const moe_config& c, int64_t T, const uint16_t* x, con
         return MOE_ERR_CUDA;
     if (!make_tma_map_2d(&tmW, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.n_experts, c.hidden, c.n_experts, kGtK))
         return MOE_ERR_CUDA;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
-    });
-    if (attr != cudaSuccess) return MOE_ERR_CUDA;
+    static PerDeviceOnce attr_once;
+    MOE_CUDA_CHECK(once_per_device(attr_once, [] {
+        return cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
+    }));
     GateTcParams p{T, c.hidden, c.n_experts, c.n_group, c.topk_group, c.top_k, c.routed_scaling_factor,
                    bias, idx, w, counts};
     gate_tc_kernel<<<static_cast<unsigned>(ceil_div(T, kGtM)), kGtThreads, kGtSmem, s>>>(tmX, tmW, p);

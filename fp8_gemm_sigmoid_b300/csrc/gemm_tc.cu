@@ -561,14 +561,12 @@ bool make_tma_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype
 }
 
 int device_sm_count() {
-    static int n = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    });
-    return n > 0 ? n : 148;
+    static PerDeviceOnce once;
+    static int n[PerDeviceOnce::kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= PerDeviceOnce::kMaxDevices) return 148;
+    (void)once_per_device(once, [dev] { return cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev); });
+    return n[dev] > 0 ? n[dev] : 148;
 }
 
 namespace {
@@ -604,13 +602,10 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     p.Ws = Ws;
     p.out = out;
     p.out_s = out_s;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemMax);
-    });
-    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    static PerDeviceOnce attr_once;
+    MOE_CUDA_CHECK(once_per_device(attr_once, [] {
+        return cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    }));
     const int64_t max_tiles = (ceil_div(rows, kBM) + n_groups) * p.n_tiles_n;
     const int grid = static_cast<int>(max_tiles < device_sm_count() ? max_tiles : device_sm_count());
     const int smem = kSmemFixed + 4 * (n_groups + 1);
