@@ -36,12 +36,15 @@ def lib():
         L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]
         L.orc_quant_1x128.argtypes = [i64, i64, vp, i32, vp, vp]
+        L.orc_quant_1x128_pow2.argtypes = [i64, i64, vp, i32, vp, vp]
         L.orc_quant_128x128.argtypes = [i64, i64, i64, vp, i32, vp, vp]
+        L.orc_quant_128x128_pow2.argtypes = [i64, i64, i64, vp, i32, vp, vp]
         L.orc_gate.argtypes = [i64, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, vp,
                                vp, vp, vp, vp]
         L.orc_permute.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp]
         L.orc_bias_update.argtypes = [i32, i64, i32, vp, vp]
         L.orc_ffn_fp8.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_ffn_fp8_pow2.argtypes = L.orc_ffn_fp8.argtypes
         L.orc_ffn_f32.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp]
         L.orc_combine.argtypes = [i64, i32, i32, vp, vp, i32, vp, vp]
         _lib = L
@@ -110,21 +113,24 @@ def f32_to_e4m3(x):
 
 # ---------------------------------------------------------------- quantisation
 
-def quant_1x128(x):
+def quant_1x128(x, pow2=False):
     """[Insights into DeepSeek-V3 précis §3.2] 1x128 activation tiles.
-    x [rows, cols] float32 or BF16 bits -> (codes uint8 [rows, cols], scales f32 [rows, cols/128])."""
+    x [rows, cols] float32 or BF16 bits -> (codes uint8 [rows, cols], scales f32 [rows, cols/128]).
+    pow2: power-of-two scales (the microscaling form the précis recommends), see moe_oracle.c."""
     x = np.ascontiguousarray(x)
     rows, cols = x.shape
     assert cols % 128 == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 128), np.float32)
-    lib().orc_quant_1x128(rows, cols, _p(x), _is_bf16(x), _p(q), _p(s))
+    fn = lib().orc_quant_1x128_pow2 if pow2 else lib().orc_quant_1x128
+    fn(rows, cols, _p(x), _is_bf16(x), _p(q), _p(s))
     return q, s
 
 
-def quant_128x128(w):
+def quant_128x128(w, pow2=False):
     """[Insights into DeepSeek-V3 précis §3.2] 128x128 weight blocks.
-    w [n, rows, cols] -> (codes [n, rows, cols], scales f32 [n, rows/128, cols/128])."""
+    w [n, rows, cols] -> (codes [n, rows, cols], scales f32 [n, rows/128, cols/128]).
+    pow2: power-of-two scales, as in quant_1x128."""
     w = np.ascontiguousarray(w)
     if w.ndim == 2:
         w = w[None]
@@ -132,7 +138,8 @@ def quant_128x128(w):
     assert rows % 128 == 0 and cols % 128 == 0
     q = np.empty((n, rows, cols), np.uint8)
     s = np.empty((n, rows // 128, cols // 128), np.float32)
-    lib().orc_quant_128x128(n, rows, cols, _p(w), _is_bf16(w), _p(q), _p(s))
+    fn = lib().orc_quant_128x128_pow2 if pow2 else lib().orc_quant_128x128
+    fn(n, rows, cols, _p(w), _is_bf16(w), _p(q), _p(s))
     return q, s
 
 
@@ -186,10 +193,11 @@ def bias_update(counts, bias, T, top_k):
 
 # ---------------------------------------------------------------- experts, combine
 
-def ffn_fp8(aq, as_, row_expert, W13q, W13s, W2q, W2s, want_h=False):
+def ffn_fp8(aq, as_, row_expert, W13q, W13s, W2q, W2s, want_h=False, pow2=False):
     """[teardown §5.1; précis §3.2] SwiGLU expert rows with blockwise FP8 operands.
     aq [n,H] codes, as_ [n,H/128]; row_expert [n] -> y [n,H] BF16 bits
-    (and, if want_h, a dict with gu f32 [n,2I], h f32 [n,I], hq [n,I], hs [n,I/128])."""
+    (and, if want_h, a dict with gu f32 [n,2I], h f32 [n,I], hq [n,I], hs [n,I/128]).
+    pow2: h is re-quantised with power-of-two scales (operands quantised with pow2=True)."""
     aq = _c(aq, np.uint8)
     as_ = _c(as_, np.float32)
     row_expert = _c(row_expert, np.int32)
@@ -202,8 +210,9 @@ def ffn_fp8(aq, as_, row_expert, W13q, W13s, W2q, W2s, want_h=False):
     h = np.empty((n, I), np.float32) if want_h else None
     hq = np.empty((n, I), np.uint8) if want_h else None
     hs = np.empty((n, I // 128), np.float32) if want_h else None
-    lib().orc_ffn_fp8(n, H, I, _p(aq), _p(as_), _p(row_expert), _p(W13q), _p(W13s), _p(W2q),
-                      _p(W2s), _p(gu), _p(h), _p(hq), _p(hs), _p(y))
+    fn = lib().orc_ffn_fp8_pow2 if pow2 else lib().orc_ffn_fp8
+    fn(n, H, I, _p(aq), _p(as_), _p(row_expert), _p(W13q), _p(W13s), _p(W2q),
+       _p(W2s), _p(gu), _p(h), _p(hq), _p(hs), _p(y))
     if want_h:
         return y, dict(gu=gu, h=h, hq=hq, hs=hs)
     return y
@@ -250,10 +259,10 @@ def round_bf16(x):
 
 # ---------------------------------------------------------------- whole layer
 
-def quantize_weights(W13, W2):
+def quantize_weights(W13, W2, pow2=False):
     """Blockwise-quantise the stacked expert weights once (oracle side)."""
-    W13q, W13s = quant_128x128(W13)
-    W2q, W2s = quant_128x128(W2)
+    W13q, W13s = quant_128x128(W13, pow2)
+    W2q, W2s = quant_128x128(W2, pow2)
     return W13q, W13s, W2q, W2s
 
 
@@ -269,7 +278,8 @@ def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     depends only on its own token, so a sample is exact.
 
     cfg: dict with hidden, inter, n_experts, n_group, topk_group, top_k,
-    routed_scaling_factor, has_shared, mode ('fp32' | 'fp8').  x [T,H] (f32 or BF16 bits);
+    routed_scaling_factor, has_shared, mode ('fp32' | 'fp8' | 'fp8_pow2': FP8 with
+    power-of-two block scales).  x [T,H] (f32 or BF16 bits);
     W13 [E(+1),2I,H], W2 [E(+1),H,I] (the shared expert is the last slot), as arrays or as
     callables ids -> stacked rows.  In fp8 mode `qweights(ids)` may return
     quantize_weights(W13[ids], W2[ids]) from a cache.  Only the experts the sample touches
@@ -296,14 +306,15 @@ def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     if n == 0:
         out.update(y=np.empty((0, x.shape[1]), x.dtype), yexp=None)
         return out
-    if cfg["mode"] == "fp8":
-        xq, xs = quant_1x128(np.ascontiguousarray(x[sample]))
+    if cfg["mode"] in ("fp8", "fp8_pow2"):
+        pow2 = cfg["mode"] == "fp8_pow2"
+        xq, xs = quant_1x128(np.ascontiguousarray(x[sample]), pow2)
         if qweights is not None:
             qw = qweights(needed)
         else:
-            qw = quantize_weights(_take(W13, needed), _take(W2, needed))
+            qw = quantize_weights(_take(W13, needed), _take(W2, needed), pow2)
         rep = np.repeat(np.arange(n), K + hs)
-        yrows = ffn_fp8(xq[rep], xs[rep], local, *qw).reshape(n, K + hs, -1)
+        yrows = ffn_fp8(xq[rep], xs[rep], local, *qw, pow2=pow2).reshape(n, K + hs, -1)
         acc = combine(yrows[:, :K], g["topk_w"][sample],
                       np.ascontiguousarray(yrows[:, K]) if hs else None)
         out.update(y=round_bf16(acc), yexp=yrows, xq=xq, xs=xs)

@@ -25,6 +25,11 @@
  *  - ties in every top-k go to the lower index; slots are in descending selection score;
  *  - a block scale is amax/448 in FP32 (amax == 0 gives scale 1 and all-zero codes), and
  *    values are encoded as e4m3(v * (448/amax)) with round-to-nearest-even and saturation;
+ *  - power-of-two mode (the *_pow2 entry points): [P2 §3.2] recommends tensor cores that
+ *    take the scaling factors natively, as Blackwell's microscaling does, and microscaling
+ *    scales are powers of two (an 8-bit exponent, 2^-127 .. 2^127).  The scale of a tile or
+ *    block is then the smallest power of two s with 448 * s >= amax, clamped to that range,
+ *    so no value saturates; codes = e4m3(v * 2^-e), an exact scaling (amax == 0 as above);
  *  - the expert FFN is SwiGLU: down(silu(gate(x)) * up(x)), no biases, gate rows 0..I-1
  *    and up rows I..2I-1 of the stacked first weight;
  *  - h goes from FP32 straight to FP8 1x128 tiles; expert outputs are BF16 and unweighted;
@@ -153,14 +158,38 @@ void orc_set_num_threads(int n)
 /* [P2 §3.2] fine-grained quantisation                                                   */
 /* ------------------------------------------------------------------------------------ */
 
+/* Exponent e of the power-of-two scale of a tile with amax > 0: the smallest integer with
+ * 448 * 2^e >= amax (448 * 2^e is exact in double), clamped to [-127, 127], the range of an
+ * 8-bit power-of-two scale. */
+static int pow2_exponent(float amax)
+{
+    const double a = (double)amax;
+    int e = (int)ceil(log2(a / 448.0));  /* first guess; corrected exactly below */
+    while (e > -127 && ldexp(448.0, e - 1) >= a) --e;
+    while (e < 127 && ldexp(448.0, e) < a) ++e;
+    if (e < -127) e = -127;
+    return e;
+}
+
 /* Encode one tile of n values (v[i*stride]) given its amax; writes codes and returns the
- * FP32 scale.  scale = amax/448; codes = e4m3(v * (448/amax)); amax == 0 -> scale 1. */
-static float quant_tile(float amax, const void* src, int64_t base, int is_bf16, int64_t n,
+ * FP32 scale.  scale = amax/448; codes = e4m3(v * (448/amax)); amax == 0 -> scale 1.
+ * pow2 != 0: scale = 2^e (pow2_exponent), codes = e4m3(v * 2^-e). */
+static float quant_tile(float amax, int pow2, const void* src, int64_t base, int is_bf16, int64_t n,
                         int64_t stride, uint8_t* dst, int64_t dbase, int64_t dstride)
 {
     if (amax == 0.0f) {
         for (int64_t i = 0; i < n; ++i) dst[dbase + i * dstride] = 0;
         return 1.0f;
+    }
+    if (pow2) {
+        /* v * 2^-e is exact wherever the product is a normal float; below that the code is 0
+         * whichever way the product rounds (E4M3's smallest step is 2^-9). */
+        const int e = pow2_exponent(amax);
+        for (int64_t i = 0; i < n; ++i) {
+            float v = load_elem(src, is_bf16, base + i * stride);
+            dst[dbase + i * dstride] = orc_f32_to_e4m3((float)ldexp((double)v, -e));
+        }
+        return (float)ldexp(1.0, e);
     }
     float mul = 448.0f / amax;
     for (int64_t i = 0; i < n; ++i) {
@@ -172,8 +201,8 @@ static float quant_tile(float amax, const void* src, int64_t base, int is_bf16, 
 
 /* Activations: one scale per row per 128 consecutive columns.
  * x [rows, cols] (cols % 128 == 0) -> q [rows, cols] E4M3 codes, s [rows, cols/128]. */
-void orc_quant_1x128(int64_t rows, int64_t cols, const void* x, int x_is_bf16,
-                     uint8_t* q, float* s)
+static void quant_1x128(int64_t rows, int64_t cols, const void* x, int x_is_bf16, int pow2,
+                        uint8_t* q, float* s)
 {
     int64_t nb = cols / 128;
 #pragma omp parallel for schedule(static)
@@ -185,15 +214,25 @@ void orc_quant_1x128(int64_t rows, int64_t cols, const void* x, int x_is_bf16,
                 float a = fabsf(load_elem(x, x_is_bf16, base + i));
                 if (a > amax) amax = a;
             }
-            s[r * nb + b] = quant_tile(amax, x, base, x_is_bf16, 128, 1, q, base, 1);
+            s[r * nb + b] = quant_tile(amax, pow2, x, base, x_is_bf16, 128, 1, q, base, 1);
         }
     }
 }
 
+void orc_quant_1x128(int64_t rows, int64_t cols, const void* x, int x_is_bf16, uint8_t* q, float* s)
+{
+    quant_1x128(rows, cols, x, x_is_bf16, 0, q, s);
+}
+
+void orc_quant_1x128_pow2(int64_t rows, int64_t cols, const void* x, int x_is_bf16, uint8_t* q, float* s)
+{
+    quant_1x128(rows, cols, x, x_is_bf16, 1, q, s);
+}
+
 /* Weights: one scale per 128x128 block of each matrix.
  * w [n_mats, rows, cols] (rows, cols % 128 == 0) -> q same shape, s [n_mats, rows/128, cols/128]. */
-void orc_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const void* w, int w_is_bf16,
-                       uint8_t* q, float* s)
+static void quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const void* w, int w_is_bf16,
+                          int pow2, uint8_t* q, float* s)
 {
     int64_t rb = rows / 128, cb = cols / 128;
 #pragma omp parallel for collapse(2) schedule(static)
@@ -209,12 +248,24 @@ void orc_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const void* w
                     }
                 float scale = 1.0f;
                 for (int64_t r = 0; r < 128; ++r)
-                    scale = quant_tile(amax, w, base + r * cols, w_is_bf16, 128, 1, q,
+                    scale = quant_tile(amax, pow2, w, base + r * cols, w_is_bf16, 128, 1, q,
                                        base + r * cols, 1);
                 s[(m * rb + i) * cb + j] = scale;
             }
         }
     }
+}
+
+void orc_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const void* w, int w_is_bf16,
+                       uint8_t* q, float* s)
+{
+    quant_128x128(n_mats, rows, cols, w, w_is_bf16, 0, q, s);
+}
+
+void orc_quant_128x128_pow2(int64_t n_mats, int64_t rows, int64_t cols, const void* w, int w_is_bf16,
+                            uint8_t* q, float* s)
+{
+    quant_128x128(n_mats, rows, cols, w, w_is_bf16, 1, q, s);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -390,10 +441,10 @@ static double block_dot(int K, const double* a_dq, const float* a_s, const uint8
  * aq [n_rows, H] codes, as [n_rows, H/128]; W13 [nE, 2I, H], W13s [nE, 2I/128, H/128];
  * W2 [nE, H, I], W2s [nE, H/128, I/128].  gu_out [n_rows, 2I] (g then u, FP32),
  * h_out [n_rows, I] (FP32), hq_out/hs_out: each may be NULL; y_out [n_rows, H] BF16 bits. */
-void orc_ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* as,
-                 const int32_t* row_expert, const uint8_t* W13, const float* W13s,
-                 const uint8_t* W2, const float* W2s, float* gu_out, float* h_out,
-                 uint8_t* hq_out, float* hs_out, uint16_t* y_out)
+static void ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* as,
+                    const int32_t* row_expert, const uint8_t* W13, const float* W13s,
+                    const uint8_t* W2, const float* W2s, int pow2, float* gu_out, float* h_out,
+                    uint8_t* hq_out, float* hs_out, uint16_t* y_out)
 {
     double lut[256];
     for (int c = 0; c < 256; ++c) lut[c] = orc_e4m3_to_double((uint8_t)c);
@@ -425,7 +476,7 @@ void orc_ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* a
                     gu_out[r * 2 * I + I + j] = u;
                 }
             }
-            orc_quant_1x128(1, I, h, 0, hq, hs);
+            quant_1x128(1, I, h, 0, pow2, hq, hs);
             for (int k = 0; k < I; ++k) h_dq[k] = lut[hq[k]];
             for (int n = 0; n < H; ++n) {
                 float y = (float)block_dot(I, h_dq, hs, w2 + (int64_t)n * I,
@@ -438,6 +489,24 @@ void orc_ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* a
         }
         free(a_dq); free(h_dq); free(h); free(hq); free(hs);
     }
+}
+
+void orc_ffn_fp8(int64_t n_rows, int H, int I, const uint8_t* aq, const float* as,
+                 const int32_t* row_expert, const uint8_t* W13, const float* W13s,
+                 const uint8_t* W2, const float* W2s, float* gu_out, float* h_out,
+                 uint8_t* hq_out, float* hs_out, uint16_t* y_out)
+{
+    ffn_fp8(n_rows, H, I, aq, as, row_expert, W13, W13s, W2, W2s, 0, gu_out, h_out, hq_out, hs_out, y_out);
+}
+
+/* The same with h re-quantised in power-of-two mode (the operands come quantised by the
+ * *_pow2 entry points; the blockwise sum itself is the same for either kind of scale). */
+void orc_ffn_fp8_pow2(int64_t n_rows, int H, int I, const uint8_t* aq, const float* as,
+                      const int32_t* row_expert, const uint8_t* W13, const float* W13s,
+                      const uint8_t* W2, const float* W2s, float* gu_out, float* h_out,
+                      uint8_t* hq_out, float* hs_out, uint16_t* y_out)
+{
+    ffn_fp8(n_rows, H, I, aq, as, row_expert, W13, W13s, W2, W2s, 1, gu_out, h_out, hq_out, hs_out, y_out);
 }
 
 /* The same expert FFN with every operand in FP32 and no quantisation (the all-FP32 layer):

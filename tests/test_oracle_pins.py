@@ -471,7 +471,7 @@ def _tiny_layer(rng, mode):
     return cfg, x, Wg, b, W13, W2
 
 
-@pytest.mark.parametrize("mode", ["fp32", "fp8"])
+@pytest.mark.parametrize("mode", ["fp32", "fp8", "fp8_pow2"])
 def test_forward_sample_is_exact_and_shared_only_when_routed_zero(orc, mode):
     rng = np.random.default_rng(13)
     cfg, x, Wg, b, W13, W2 = _tiny_layer(rng, mode)
@@ -487,8 +487,10 @@ def test_forward_sample_is_exact_and_shared_only_when_routed_zero(orc, mode):
         sh = orc.ffn_f32(x, np.full(x.shape[0], 16, np.int32), W13, W2)
         assert np.array_equal(z["y"], sh)
     else:
-        xq, xs = orc.quant_1x128(x)
-        sh = orc.ffn_fp8(xq, xs, np.full(x.shape[0], 16, np.int32), *orc.quantize_weights(W13, W2))
+        pow2 = mode == "fp8_pow2"
+        xq, xs = orc.quant_1x128(x, pow2)
+        sh = orc.ffn_fp8(xq, xs, np.full(x.shape[0], 16, np.int32), *orc.quantize_weights(W13, W2, pow2),
+                         pow2=pow2)
         assert np.array_equal(z["y"], sh)
 
 
@@ -500,3 +502,124 @@ def test_forward_top1_weight_is_scaled_score(orc):
     g = orc.gate(x, Wg, b, 4, 2, 1, 2.5, want_scores=True)
     s = np.take_along_axis(g["scores"], g["topk_idx"], 1)[:, 0]
     assert np.array_equal(out["topk_w"][:, 0], s * np.float32(2.5))
+
+
+# ------------------------------------------------------------------ power-of-two scales
+# Insights into DeepSeek-V3 (précis) §3.2 recommends tensor cores that take the scaling
+# factors natively (Blackwell's microscaling), whose scales are powers of two.  The oracle's
+# power-of-two mode takes the smallest power of two s with 448*s >= amax, clamped to
+# 2^-127 .. 2^127, and encodes v * 2^-e.
+
+def _check_pow2_tile(tile, codes, scale, table):
+    amax = float(np.max(np.abs(tile)))
+    if amax == 0:
+        assert scale == 1.0 and not codes.any()
+        return
+    m, e2 = np.frexp(np.float64(scale))
+    assert m == 0.5, scale                      # an exact power of two
+    e = int(e2) - 1
+    assert -127 <= e <= 127
+    assert 448.0 * 2.0 ** e >= amax             # covers the tile: nothing saturates
+    if e > -127:
+        assert 448.0 * 2.0 ** (e - 1) < amax    # and is the smallest such power
+        assert amax * 2.0 ** -e > 224.0         # so amax lands in the top binade of E4M3
+    scaled = tile.astype(np.float64) * 2.0 ** -e  # exact
+    assert np.max(np.abs(scaled)) <= 448.0
+    ref = torch.from_numpy(scaled.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    # dequantised error within half a code step
+    dq = table[codes] * np.float64(scale)
+    step = np.array([_e4m3_gap(table, abs(float(v))) for v in scaled]) * np.float64(scale)
+    assert np.all(np.abs(dq - tile) <= 0.5 * step * (1 + 1e-12) + 1e-300)
+
+
+def test_pow2_quant_1x128_scales_and_codes(orc):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((7, 512)).astype(np.float32)
+    x[0, :128] *= np.float32(1e-3)
+    x[1, 128:256] = 0.0                                            # all-zero tile
+    x[2, :128] = np.clip(x[2, :128], -1, 1)
+    x[2, 5] = np.float32(448 * 2.0 ** -3)                          # amax exactly 448 * 2^-3
+    x[3, :128] = np.clip(x[3, :128], -1, 1)
+    x[3, 7] = np.nextafter(np.float32(448 * 2.0 ** -2), np.float32(np.inf))  # just above 448 * 2^-2
+    x[4, 256:384] = np.float32(2.0) ** rng.integers(-20, 20, 128).astype(np.float32)
+    x[5, 384:] *= np.float32(1e-37)                                # exponent clamped at -127
+    x[6, :128] = np.float32(-448 * 2.0 ** 5)                       # constant negative tile
+    q, s = orc.quant_1x128(x, pow2=True)
+    table = orc.e4m3_table()
+    for r in range(x.shape[0]):
+        for b in range(4):
+            _check_pow2_tile(x[r, b * 128:(b + 1) * 128], q[r, b * 128:(b + 1) * 128], float(s[r, b]), table)
+    assert s[2, 0] == np.float32(2.0 ** -3) and q[2, 5] == 0x7E     # amax -> code 448
+    assert s[3, 0] == np.float32(2.0 ** -1)
+    assert s[5, 3] == np.float32(2.0 ** -127)
+    assert s[6, 0] == np.float32(2.0 ** 5) and np.all(q[6, :128] == 0xFE)
+    # BF16 input reads the same values as the FP32 path
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    qb, sb = orc.quant_1x128(xb.view(torch.uint16).numpy(), pow2=True)
+    qf, sf = orc.quant_1x128(xb.float().numpy(), pow2=True)
+    assert np.array_equal(qb, qf) and np.array_equal(sb, sf)
+
+
+def test_pow2_quant_128x128_block_layout(orc):
+    rng = np.random.default_rng(22)
+    n, R, C = 2, 256, 384
+    w = rng.standard_normal((n, R, C)).astype(np.float32)
+    # every block its own magnitude (not a power of two apart), so a transposed or shifted
+    # block index shows in the scales
+    for m in range(n):
+        for i in range(R // 128):
+            for j in range(C // 128):
+                w[m, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128] *= np.float32(3.0 ** (i + 2 * j + 5 * m - 6))
+    w[1, :128, 128:256] = 0.0
+    q, s = orc.quant_128x128(w, pow2=True)
+    table = orc.e4m3_table()
+    for m in range(n):
+        for i in range(R // 128):
+            for j in range(C // 128):
+                blk = w[m, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+                qb = q[m, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+                sc = float(s[m, i, j])
+                for r in range(0, 128, 37):      # rows of the block share its one scale
+                    amax = float(np.abs(blk).max())
+                    if amax == 0:
+                        assert sc == 1.0 and not qb.any()
+                        continue
+                    e = int(np.frexp(np.float64(sc))[1]) - 1
+                    assert 448.0 * 2.0 ** e >= amax > 448.0 * 2.0 ** (e - 1)
+                    scaled = blk[r].astype(np.float64) * 2.0 ** -e
+                    ref = torch.from_numpy(scaled.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                    assert np.array_equal(qb[r], ref)
+    assert len({float(v) for v in s.ravel()}) > 6
+
+
+def test_pow2_ffn_against_dense_float64_matmul(orc):
+    # the blockwise sum is the same for either kind of scale: g, u and y still equal the
+    # float64 matmul of the dequantised operands, and h is re-quantised with power-of-two scales
+    rng = np.random.default_rng(23)
+    n, H, I, nE = 5, 384, 256, 2
+    x, W13, W2 = _tiny_fp8_expert_case(rng, n, H, I, nE)
+    xq, xs = orc.quant_1x128(x, pow2=True)
+    W13q, W13s, W2q, W2s = orc.quantize_weights(W13, W2, pow2=True)
+    row_e = np.array([0, 1, 1, 0, 1], np.int32)
+    y, aux = orc.ffn_fp8(xq, xs, row_e, W13q, W13s, W2q, W2s, want_h=True, pow2=True)
+    t = orc.e4m3_table()
+    A = _dequant(t, xq, xs, 1, 128)
+    for r in range(n):
+        e = row_e[r]
+        gu = (A[r] @ _dequant(t, W13q[e], W13s[e], 128, 128).T).astype(np.float32)
+        assert np.array_equal(aux["gu"][r], gu), r
+        h = (torch.nn.functional.silu(torch.from_numpy(gu[:I]).double()).numpy()
+             * gu[I:].astype(np.float64)).astype(np.float32)
+        assert np.array_equal(aux["h"][r], h)
+        for b in range(I // 128):
+            _check_pow2_tile(h[b * 128:(b + 1) * 128], aux["hq"][r, b * 128:(b + 1) * 128],
+                             float(aux["hs"][r, b]), t)
+        Hd = _dequant(t, aux["hq"][r][None], aux["hs"][r][None], 1, 128)[0]
+        yref = torch.from_numpy((_dequant(t, W2q[e], W2s[e], 128, 128) @ Hd).astype(np.float32)) \
+            .to(torch.bfloat16).view(torch.uint16).numpy()
+        assert np.array_equal(y[r], yref)
+    # the FP32-scale mode quantises the same h differently (its scale is amax/448)
+    _, aux32 = orc.ffn_fp8(xq, xs, row_e, W13q, W13s, W2q, W2s, want_h=True, pow2=False)
+    assert np.array_equal(aux32["gu"], aux["gu"]) and not np.array_equal(aux32["hs"], aux["hs"])
+
