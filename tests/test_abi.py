@@ -113,3 +113,40 @@ def test_pipeline_host_side_checks(moe):
     assert not h.value
     assert L.moe_pipeline_submit(None, 1, None, None, None, 0, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_pipeline_destroy(None) == moe.MOE_OK
+
+
+def _header_prototypes():
+    """name -> list of parameter type strings, from every MOE_API prototype in moe.h."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        # drop the parameter name, keep the type
+        protos[m.group(1)] = [re.sub(r"\b\w+\s*$", "", p).strip() for p in params]
+    return protos
+
+
+def _ctypes_kind(t):
+    if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int32: "int32_t", ctypes.c_int64: "int64_t", ctypes.c_size_t: "size_t",
+            ctypes.c_float: "float"}[t]
+
+
+def _c_kind(t):
+    if "*" in t or t in ("moe_stream_t",):
+        return "ptr"
+    return {"int32_t": "int32_t", "int64_t": "int64_t", "size_t": "size_t", "float": "float"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    # every entry point the binding calls: same parameter count, and the same width for
+    # every scalar (an int64 size passed as int32 would corrupt the call silently)
+    from fp8_gemm_sigmoid_b300 import moe as m
+    protos = _header_prototypes()
+    assert set(m._SIGS) <= set(protos), set(m._SIGS) - set(protos)
+    for name, sig in m._SIGS.items():
+        c = [_c_kind(t) for t in protos[name]]
+        py = [_ctypes_kind(t) for t in sig]
+        assert c == py, (name, c, py)
