@@ -150,3 +150,48 @@ def test_binding_signatures_match_the_header():
         c = [_c_kind(t) for t in protos[name]]
         py = [_ctypes_kind(t) for t in sig]
         assert c == py, (name, c, py)
+
+
+def test_more_host_side_rejections(moe):
+    # every case below is refused before any CUDA call, so it runs without a GPU
+    L = moe._lib_handle()
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    cfg = moe.make_config(sy.config("v3_prefill"))
+    bad_cfg = moe.make_config(dict(sy.config("v3_prefill"), n_group=7))
+    c, cb = ctypes.byref(cfg), ctypes.byref(bad_cfg)
+    INV = moe.MOE_ERR_INVALID_ARG
+    # gate
+    assert L.moe_gate(c, -1, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
+    assert L.moe_gate(c, 8, vp(16), vp(16), vp(16), vp(16), vp(16), None, None) == INV
+    assert L.moe_gate(cb, 8, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
+    assert L.moe_gate(c, 8, None, vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
+    # combine: T == 0 enqueues nothing and succeeds; missing or misaligned buffers are refused
+    assert L.moe_combine(c, 0, None, None, None, None, None) == moe.MOE_OK
+    assert L.moe_combine(c, 8, None, vp(16), vp(16), vp(16), None) == INV
+    assert L.moe_combine(c, 8, vp(16), vp(16), vp(16), vp(24), None) == INV
+    # bias update
+    assert L.moe_bias_update(c, 8, vp(16), None, None) == INV
+    assert L.moe_bias_update(c, -1, vp(16), vp(16), None) == INV
+    # whole layer: missing weights, a misaligned or short workspace
+    need = ctypes.c_size_t(0)
+    assert L.moe_workspace_size(c, 64, ctypes.byref(need)) == moe.MOE_OK
+    w = moe.moe_weights(vp(16), vp(16), vp(16), vp(16), vp(16))
+    w_missing = moe.moe_weights(vp(16), None, vp(16), vp(16), vp(16))
+    args = lambda ww, ws, nb: (c, 64, vp(16), ctypes.byref(ww), vp(16), 0, vp(16), vp(16), vp(16),  # noqa: E731
+                               vp(16), ws, nb, None)
+    assert L.moe_forward(*args(w_missing, vp(1024), need.value)) == INV
+    assert L.moe_forward(*args(w, vp(1032 + 1), need.value)) == INV
+    assert L.moe_forward(*args(w, vp(1024), need.value - 1)) == moe.MOE_ERR_WORKSPACE
+    # the no-allocation permutation: beyond its fixed scratch (2 * ceil(T/64) * E > 2^20)
+    f = L.moe_permute_noalloc
+    f.argtypes = [moe._cfgp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    f.restype = ctypes.c_int
+    assert f(c, 200000, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) \
+        == moe.MOE_ERR_UNSUPPORTED
+    assert f(c, 100, vp(16), vp(16), vp(16), None, vp(16), vp(16), vp(16), vp(16), None) == INV
+    assert f(c, 100, vp(16), vp(17), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
+    # the bounded-wait self-test refuses budgets outside 1 .. 4e9 cycles
+    assert L.moe_selftest_wait_timeout(0, None) == INV
+    assert L.moe_selftest_wait_timeout(4000000001, None) == INV
+    assert L.moe_device_error(None) == INV
