@@ -11,6 +11,7 @@ With N > 1 (torchrun), every rank runs its own T tokens (independent replicas, w
 scaling; the layer has no cross-token exchange) and the slowest rank's time counts.
 """
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -31,6 +32,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gate": "gate.cu",
                   "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu"}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
+STAGED_SECONDS = 2.5  # the per-stage pass runs at least this long (>= 20 clock samples)
 
 # kernels each entry point launches in the FP8 layer (memsets excluded); summed into
 # gpu_launches.  moe_permute: chunk histogram, scan, positions, row gather, scale gather.
@@ -47,9 +49,16 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--config", default="v3_prefill", choices=sorted(sy.CONFIGS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle's timed sample")
+    p.add_argument("--cpu-sample", type=int, default=512,
+                   help="tokens of the seeded sample on which the oracle's expert FFNs are timed")
+    p.add_argument("--ref-gate-tokens", type=int, default=2048,
+                   help="reference arm: tokens per step through the oracle's gate")
+    p.add_argument("--ref-sample", type=int, default=64,
+                   help="reference arm: tokens per step through the oracle's expert FFNs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--staged-seconds", type=float, default=STAGED_SECONDS,
+                   help="minimum length of the per-stage pass (0: exactly --steps steps, for profiling)")
     # smaller variants of the workload for profiler captures (same per-expert row count
     # when T*top_k/experts is kept)
     p.add_argument("--T", type=int, default=None)
@@ -72,24 +81,37 @@ def load_peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons, started before the timed regions;
+    stats(t0, t1) summarises the samples whose timestamps fall inside one region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, index):
         self.index = index
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.rows = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
+        # wait (bounded) for the first sample, so that the timed regions are covered
+        t_end = time.time() + 10
+        while self.p is not None and time.time() < t_end:
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.05)
+
+    @staticmethod
+    def now():
+        return datetime.datetime.now()
 
     def stop(self):
         if self.p is None:
-            return None
+            return
         self.p.terminate()
         self.p.wait()
         self.f.flush()
@@ -97,20 +119,38 @@ class Clocks:
         with open(self.f.name) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                except ValueError:
+                    continue
+                rows.append([ts] + parts[1:])
         os.unlink(self.f.name)
+        self.rows = rows
+
+    def stats(self, t0, t1):
+        if not self.rows:
+            return None
+        rows = [r for r in self.rows if t0 <= r[0] <= t1]
+        if not rows:  # a region shorter than one period: the samples around it
+            before = [r for r in self.rows if r[0] < t0][-1:]
+            after = [r for r in self.rows if r[0] > t1][:1]
+            rows = before + after
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        num = lambda v: v.replace(".", "").isdigit()  # noqa: E731
+        sm = [float(r[2]) for r in rows if num(r[2])]
+        pw = [float(r[4]) for r in rows if num(r[4])]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
-            for n, v in zip(names, r[5:9]):
+            for n, v in zip(names, r[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "sm_max_mhz": float(rows[0][3]) if num(rows[0][3]) else None,
+                "power_w_max": max(pw) if pw else None,
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
@@ -172,7 +212,8 @@ class Layer:
         moe.moe_grouped_gemm_fp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
                                  self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None, self.ws)
         ev[5].record()
-        moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], self.y)
+        ysh = self.yexp[T * c["top_k"]:] if c["has_shared"] else None
+        moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], ysh, self.y)
         ev[6].record()
         if c["update_bias"]:
             moe.moe_bias_update(c, T, o["counts"], self.bias)
@@ -201,23 +242,29 @@ def stage_work(cfg):
     }
 
 
-def measured_traffic(stage, workload):
-    """DRAM bytes (read + write) of one launch of the stage's kernel, from the ncu counters in
-    profiles/dram_traffic.txt, or None when none were taken for this workload or the kernel's
-    source has changed since (the file records the source's SHA-256)."""
+def measured_traffic(stage, cfg):
+    """DRAM bytes (read + write) of one launch of the stage's kernel on cfg's workload, from the
+    ncu counters recorded in profiles/dram_traffic.txt, or (None, None) when no capture of the
+    kernel's current source exists.  A capture is taken on a cut-down case of the workload's
+    shape (fewer tokens and experts, the same rows per expert); its bytes scale to cfg's
+    workload by the tokens processed.  Each line of the file records the SHA-256 of the
+    kernel's source at capture time, and a line only counts while the source is unchanged."""
     import hashlib
     src = KERNEL_SOURCES.get(stage)
     if src is None or not os.path.exists(TRAFFIC_FILE):
-        return None
+        return None, None
     with open(os.path.join(ROOT, "fp8_gemm_sigmoid_b300", "csrc", src), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 5 and not line.startswith("#") and parts[0] == workload and parts[1] == stage:
-                if parts[2] == sha:
-                    return int(parts[3]) + int(parts[4])
-    return None
+            if line.startswith("#") or len(parts) < 7:
+                continue
+            workload, st, digest, rd, wr, cap_T, cap_E = parts[:7]
+            if workload == cfg["name"] and st == stage and digest == sha and int(cap_E) * cfg["T"] == int(cap_T) * cfg["n_experts"]:
+                scale = cfg["T"] / int(cap_T)
+                return int(round((int(rd) + int(wr)) * scale)), "ncu capture at T=%s E=%s scaled by tokens x%.3g" % (cap_T, cap_E, scale)
+    return None, None
 
 
 def barrier_sync(dist_on):
@@ -245,38 +292,132 @@ def replica_throughput(tokens_per_rank, steps, ms_per_rank, dist_on):
     return world * tokens_per_rank * steps / (ms / 1e3), ms
 
 
-def cpu_baseline(cfg, layer, n_tok):
-    """The oracle, as it stands, on a bounded sample: the first n_tok tokens as a layer of its
-    own (gate, permutation, expert FFNs, combine).  Weight quantisation is offline on both
-    sides, so it is done before timing, for the experts the sample touches."""
-    import numpy as np
-    import oracle
+class OracleLayer:
+    """The CPU oracle on the workload's inputs (host copies), with the expert weights it needs
+    quantised on the oracle side beforehand: quantisation of the weights is an offline step on
+    both sides, so no timed region contains it."""
 
-    sub = dict(cfg, T=n_tok)
-    x = layer.inp["x"][:n_tok].view(torch.uint16).cpu().numpy()
-    Wg = layer.inp["Wg"].view(torch.uint16).cpu().numpy()
-    bias = layer.inp["bias"].cpu().numpy()
-    W13, W2 = layer.inp["W13"], layer.inp["W2"]
+    def __init__(self, cfg, layer):
+        import numpy as np
+        import oracle
+        self.np, self.oracle, self.cfg = np, oracle, cfg
+        self.x = layer.inp["x"].view(torch.uint16).cpu().numpy()
+        self.Wg = layer.inp["Wg"].view(torch.uint16).cpu().numpy()
+        self.bias = layer.inp["bias"].cpu().numpy()
+        self.W13, self.W2 = layer.inp["W13"], layer.inp["W2"]
+        self.cache = {}
 
-    def qfn(ids, cache={}):
-        miss = [int(e) for e in ids if int(e) not in cache]
+    def qweights(self, ids):
+        np = self.np
+        miss = [int(e) for e in ids if int(e) not in self.cache]
         if miss:
-            idx = torch.tensor(miss, device=W13.device)
-            w13 = W13.index_select(0, idx).view(torch.uint16).cpu().numpy()
-            w2 = W2.index_select(0, idx).view(torch.uint16).cpu().numpy()
-            q = oracle.quantize_weights(w13, w2)
+            idx = torch.tensor(miss, device=self.W13.device)
+            w13 = self.W13.index_select(0, idx).view(torch.uint16).cpu().numpy()
+            w2 = self.W2.index_select(0, idx).view(torch.uint16).cpu().numpy()
+            q = self.oracle.quantize_weights(w13, w2)
             for j, e in enumerate(miss):
-                cache[e] = tuple(a[j:j + 1] for a in q)
-        return tuple(np.concatenate([cache[int(e)][i] for e in ids]) for i in range(4))
+                self.cache[e] = tuple(a[j:j + 1] for a in q)
+        return tuple(np.concatenate([self.cache[int(e)][i] for e in ids]) for i in range(4))
 
-    g = oracle.gate(x, Wg, bias, cfg["n_group"], cfg["topk_group"], cfg["top_k"],
-                    cfg["routed_scaling_factor"])
-    ids = np.unique(np.concatenate([g["topk_idx"].ravel(), [cfg["n_experts"]]]))
-    qfn(ids)  # quantise outside the timed region
-    t0 = time.perf_counter()
-    oracle.forward(sub, x, Wg, bias, None, None, qweights=qfn)
-    dt = time.perf_counter() - t0
-    return dt, oracle.num_threads()
+    def gate(self, tokens):
+        c = self.cfg
+        return self.oracle.gate(self.x[tokens], self.Wg, self.bias, c["n_group"], c["topk_group"], c["top_k"],
+                                c["routed_scaling_factor"])
+
+    def prepare(self, g, sample):
+        """Quantise (untimed) the experts that `sample`'s tokens of routing `g` reach."""
+        ids = self.np.unique(self.np.concatenate([g["topk_idx"][sample].ravel(), [self.cfg["n_experts"]]]))
+        self.qweights(ids)
+
+    def timed(self, gate_tokens, sample):
+        """One pass of the plan: gate and permutation over `gate_tokens` (a contiguous range of
+        the batch), then the expert FFNs and the combine for `sample` (indices into that range).
+        Returns (gate seconds, expert seconds)."""
+        c = self.cfg
+        t0 = time.perf_counter()
+        g = self.gate(gate_tokens)
+        self.oracle.permute(g["topk_idx"], c["n_experts"], int(c["has_shared"]))
+        t1 = time.perf_counter()
+        self.prepare(g, sample)
+        t2 = time.perf_counter()
+        self.oracle.experts_and_combine(c, self.x[gate_tokens], g, sample, None, None, qweights=self.qweights)
+        t3 = time.perf_counter()
+        return t1 - t0, t3 - t2
+
+
+def cpu_baseline(cfg, layer, n_sample):
+    """The oracle, as it stands, on the host cores: the gate and the permutation over all T
+    tokens, then the expert FFNs and the combine on a seeded sample of n_sample tokens.  Every
+    output row depends only on its own token, so the expert part extrapolates per token:
+    tokens/s = T / (gate time + expert time * T / n_sample)."""
+    T = cfg["T"]
+    ol = OracleLayer(cfg, layer)
+    sample = sy.sample_tokens(T, n_sample, seed=2).numpy()
+    g = ol.gate(slice(0, T))
+    ol.prepare(g, sample)  # weights quantised outside the timed passes
+    t_gate, t_exp = ol.timed(slice(0, T), sample)
+    n = len(sample)
+    value = T / (t_gate + t_exp * T / n)
+    return {"value": value, "unit": "tokens/s", "cores": ol.oracle.num_threads(), "kind": "oracle",
+            "sample": "gate + permutation over all %d tokens (%.2f s), expert FFNs + combine on a seeded "
+                      "%d-token sample (%.2f s), extrapolated per token to %d tokens"
+                      % (T, t_gate, n, t_exp, T, T)}
+
+
+def run_reference(args, cfg, rank, world):
+    """The reference arm: the CPU oracle timed on the host cores, rank 0 only.  Each step runs
+    the cpu_baseline plan on a bounded slice of the batch (gate + permutation over a run of
+    ref_gate_tokens tokens, expert FFNs + combine on a seeded sample of ref_sample of them) and
+    the per-token times extrapolate to the workload's T, as cpu_baseline's do."""
+    if rank != 0:
+        return
+    import numpy as np
+    torch.cuda.set_device(0)
+    layer = Layer(cfg, "cuda:0")
+    ol = OracleLayer(cfg, layer)
+    T = cfg["T"]
+    n_gate = min(args.ref_gate_tokens, T)
+    n_exp = min(args.ref_sample, n_gate)
+
+    def step(i):
+        start = (i * 7919 * n_gate) % max(1, T - n_gate + 1)
+        sample = np.sort(np.random.default_rng(1000 + i).choice(n_gate, n_exp, replace=False))
+        rng = slice(start, start + n_gate)
+        ol.prepare(ol.gate(rng), sample)
+        return ol.timed(rng, sample)
+
+    for i in range(args.warmup):
+        step(i)
+    per_token = 0.0
+    tot = 0.0
+    for i in range(args.steps):
+        tg, te = step(args.warmup + i)
+        per_token += tg / n_gate + te / n_exp
+        tot += tg + te
+    val = args.steps / per_token
+    line = {
+        "impl": "reference", "metric": metric_name(cfg), "value": val,
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, 1),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": ol.oracle.num_threads(), "kind": "oracle",
+                         "sample": "per step: gate + permutation over %d consecutive tokens of the %s batch, "
+                                   "expert FFNs + combine on a seeded %d-token sample of them; per-token "
+                                   "times extrapolated to the batch (the plan of cpu_baseline on a smaller "
+                                   "slice)" % (n_gate, cfg["name"], n_exp)},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def gemm_rows(counts, T, has_shared, bm=128):
+    """Rows the grouped GEMMs compute: the algorithmic rows and the rows of whole bm-row tiles."""
+    import numpy as np
+    c = np.asarray(counts, np.int64)
+    useful = int(c.sum()) + (T if has_shared else 0)
+    tiles = int(np.sum((c + bm - 1) // bm)) + ((T + bm - 1) // bm if has_shared else 0)
+    return {"useful": useful, "tile_rows": tiles * bm, "tile_efficiency": useful / max(1, tiles * bm)}
 
 
 def metric_name(cfg):
@@ -379,27 +520,35 @@ def main():
     clocks = Clocks(local)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier_sync(dist_on)
+    r1 = [clocks.now()]
     start.record(stream)
     for _ in range(args.steps):
         layer.forward()
     stop.record(stream)
     barrier_sync(dist_on)
-    clk = clocks.stop()
+    r1.append(clocks.now())
     value, ms = replica_throughput(T, args.steps, start.elapsed_time(stop), dist_on)
     assert moe.moe_device_error() == 0
 
-    # timed region 2: the same K steps through the staged entry points, per-stage events
-    # (events for every step up front and one synchronize at the end, so that the host's
-    # enqueueing never leaves the GPU idle between stages)
+    # timed region 2: the staged entry points with an event after every stage, repeated for
+    # at least STAGED_SECONDS so that the clock record holds enough samples (events for every
+    # step up front and one synchronize at the end, so that the host's enqueueing never leaves
+    # the GPU idle between stages)
+    step_s = ms / args.steps / 1e3
+    n_staged = max(args.steps, min(2000, int(args.staged_seconds / max(step_s, 1e-6)) + 1)
+                   if args.staged_seconds > 0 else args.steps)
     stage_ms = {s: 0.0 for s in Layer.STAGES}
     barrier_sync(dist_on)
-    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_staged)]
+    r2 = [clocks.now()]
     for evs in all_evs:
         layer.staged(evs)
     barrier_sync(dist_on)
+    r2.append(clocks.now())
     for evs in all_evs:
         for i, s in enumerate(Layer.STAGES):
-            stage_ms[s] += evs[i].elapsed_time(evs[i + 1]) / args.steps
+            stage_ms[s] += evs[i].elapsed_time(evs[i + 1]) / n_staged
+    counts = layer.out["counts"].cpu().numpy()
 
     # end to end through the host-buffer entry points (moe_pipeline_submit): every step
     # uploads its tokens from pinned host memory and downloads y, the routing and the
@@ -436,9 +585,14 @@ def main():
                "api": "moe_pipeline_submit (pinned host buffers)"}
         del pl
         torch.cuda.empty_cache()
+    clocks.stop()
+    clk = clocks.stats(*r1)
+    stage_clk = clocks.stats(*r2)
 
     work = stage_work(cfg)
-    fp8_peak = peaks["bf16_sus"] * FP8_PER_BF16
+    # the grouped GEMMs are timed in short regions at full clock: their denominator is the
+    # burst BF16 figure times the nominal FP8:BF16 ratio
+    fp8_peak = peaks["bf16"] * FP8_PER_BF16
     stages = {}
     for s in Layer.STAGES:
         if s == "bias_update" and not cfg["update_bias"]:
@@ -456,23 +610,22 @@ def main():
     dom_t = stage_ms[dom] / 1e3
     if kind == "tensor":
         roof = {"kernel": dom, "bound": "tensor", "achieved": amount / dom_t / 1e12, "peak": fp8_peak,
-                "unit": "TFLOP/s", "peak_source": "%s bf16 sustained x %.0f (nominal FP8:BF16)" % (peaks["src"], FP8_PER_BF16)}
+                "unit": "TFLOP/s",
+                "peak_source": "%s bf16 burst x %.0f (nominal FP8:BF16), of %s" % (
+                    peaks["src"], FP8_PER_BF16, peaks["src"])}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": amount / dom_t / 1e9, "peak": peaks["hbm"],
                 "unit": "GB/s", "peak_source": "%s copy bandwidth" % peaks["src"]}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(dom, cfg["name"] if cfg["T"] == sy.CONFIGS[cfg["name"]]["T"] else None)
+    roof["traffic"], roof["traffic_source"] = measured_traffic(dom, cfg)
     roof["algorithmic"] = amount
+    roof["sm_mhz"] = stage_clk["sm_mhz"] if stage_clk else None
     gemm_ms = stage_ms["gemm1_swiglu"] + stage_ms["gemm2_down"]
     gemm_tflops = (work["gemm1_swiglu"][1] + work["gemm2_down"][1]) / (gemm_ms / 1e3) / 1e12
 
     cpu = None
     if want_cpu:
-        n = min(args.cpu_sample, T)
-        dt, threads = cpu_baseline(cfg, layer, n)
-        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "first %d of the %d tokens as a layer of their own (gate, permutation, "
-                         "expert FFNs, combine; weights quantised beforehand)" % (n, T)}
+        cpu = cpu_baseline(cfg, layer, min(args.cpu_sample, T))
 
     line = {
         "metric": metric_name(cfg),
@@ -488,13 +641,16 @@ def main():
         "dtype": "fp8-e4m3 (FP32 accumulation), bf16 activations",
         "data": "synthetic",
         "config": config_dict(cfg, world),
-        "grouped_gemm": {"ms": gemm_ms, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
+        "grouped_gemm": {"ms": gemm_ms, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak,
+                         "rows": gemm_rows(counts, T, cfg["has_shared"])},
         "stages": stages,
+        "staged_steps": n_staged,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": layer.launches_per_step() * args.steps,
         "clocks": clk,
+        "stage_clocks": stage_clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

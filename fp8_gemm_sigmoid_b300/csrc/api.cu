@@ -192,7 +192,8 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
         MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, static_cast<int32_t>(H), static_cast<int32_t>(I),
                                      hq, hs, static_cast<const uint8_t*>(w->W2), w->W2_s,
                                      MOE_EPI_STORE, yexp, nullptr, gscratch, gbytes, stream));
-        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, y, stream));
+        const void* yshared = c.has_shared ? static_cast<const char*>(yexp) + T * c.top_k * H * 2 : nullptr;
+        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, yshared, y, stream));
     } else {
         float* aq = reinterpret_cast<float*>(base + L.aq);
         float* h = reinterpret_cast<float*>(base + L.hq);
@@ -205,7 +206,8 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
         MOE_TRY(moe_grouped_gemm_f32(G, offs, L.R, static_cast<int32_t>(H), static_cast<int32_t>(I),
                                      h, static_cast<const float*>(w->W2), MOE_EPI_STORE, yexp,
                                      gscratch, gbytes, stream));
-        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, y, stream));
+        const float* yshared = c.has_shared ? yexp + T * c.top_k * H : nullptr;
+        MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, yshared, y, stream));
     }
     return MOE_OK;
 }

@@ -4,8 +4,9 @@
 // DeepSeek-V3 co-design teardown (wsisp.com) §2.3: after the experts run, each token's rows
 // come back and are summed with its routing weights; Insights into DeepSeek-V3 précis §3.1:
 // the combine payload is BF16.  Per token and column, in FP32 and slot order:
-//   y = sum_k w[t,k] * yexp[row_of[t,k]] (+ yexp[T*K + t] for the shared expert),
-// each term a separate FP32 multiply and add, rounded once to the output type.
+//   y = sum_k w[t,k] * yexp[row_of[t,k]] (+ yshared[t] for the shared expert),
+// each term a separate FP32 multiply and add, rounded once to the output type.  A slot whose
+// row lies outside [0, T*K) (row_of = -1: an expert id the permutation dropped) adds nothing.
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,9 +15,9 @@ namespace {
 
 // One thread per (token, 8 BF16 columns): 16-byte gathered loads, 16-byte store.
 __global__ void __launch_bounds__(256)
-combine_bf16_kernel(int64_t T, int H, int K, int has_shared, const uint16_t* __restrict__ yexp,
+combine_bf16_kernel(int64_t T, int H, int K, const uint16_t* __restrict__ yexp,
                     const int32_t* __restrict__ row_of, const float* __restrict__ w,
-                    uint16_t* __restrict__ y) {
+                    const uint16_t* __restrict__ yshared, uint16_t* __restrict__ y) {
     const int chunks = H / 8;
     const int64_t total = T * chunks;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -28,6 +29,7 @@ combine_bf16_kernel(int64_t T, int H, int K, int has_shared, const uint16_t* __r
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
         for (int k = 0; k < K; ++k) {
             const int64_t r = row_of[t * K + k];
+            if (r < 0 || r >= T * K) continue;  // dropped slot
             const float wk = w[t * K + k];
             uint4 v = *reinterpret_cast<const uint4*>(yexp + r * H + ch * 8);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -38,8 +40,8 @@ combine_bf16_kernel(int64_t T, int H, int K, int has_shared, const uint16_t* __r
                     __fadd_rn(acc[2 * j + 1], __fmul_rn(wk, __uint_as_float(u[j] & 0xffff0000u)));
             }
         }
-        if (has_shared) {
-            uint4 v = *reinterpret_cast<const uint4*>(yexp + (T * K + t) * H + ch * 8);
+        if (yshared) {
+            uint4 v = *reinterpret_cast<const uint4*>(yshared + t * H + ch * 8);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -58,9 +60,9 @@ combine_bf16_kernel(int64_t T, int H, int K, int has_shared, const uint16_t* __r
 
 // FP32 rows: one thread per (token, 4 columns).
 __global__ void __launch_bounds__(256)
-combine_f32_kernel(int64_t T, int H, int K, int has_shared, const float* __restrict__ yexp,
+combine_f32_kernel(int64_t T, int H, int K, const float* __restrict__ yexp,
                    const int32_t* __restrict__ row_of, const float* __restrict__ w,
-                   float* __restrict__ y) {
+                   const float* __restrict__ yshared, float* __restrict__ y) {
     const int chunks = H / 4;
     const int64_t total = T * chunks;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -70,6 +72,7 @@ combine_f32_kernel(int64_t T, int H, int K, int has_shared, const float* __restr
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
             const int64_t r = row_of[t * K + k];
+            if (r < 0 || r >= T * K) continue;  // dropped slot
             const float wk = w[t * K + k];
             float4 v = *reinterpret_cast<const float4*>(yexp + r * H + ch * 4);
             acc.x = __fadd_rn(acc.x, __fmul_rn(wk, v.x));
@@ -77,8 +80,8 @@ combine_f32_kernel(int64_t T, int H, int K, int has_shared, const float* __restr
             acc.z = __fadd_rn(acc.z, __fmul_rn(wk, v.z));
             acc.w = __fadd_rn(acc.w, __fmul_rn(wk, v.w));
         }
-        if (has_shared) {
-            float4 v = *reinterpret_cast<const float4*>(yexp + (T * K + t) * H + ch * 4);
+        if (yshared) {
+            float4 v = *reinterpret_cast<const float4*>(yshared + t * H + ch * 4);
             acc.x = __fadd_rn(acc.x, v.x);
             acc.y = __fadd_rn(acc.y, v.y);
             acc.z = __fadd_rn(acc.z, v.z);
@@ -104,11 +107,13 @@ __global__ void bias_update_kernel(int E, int64_t T, int K, const int32_t* __res
 using namespace moe;
 
 extern "C" moe_status moe_combine(const moe_config* cfg, int64_t T, const void* yexp,
-                                  const int32_t* row_of, const float* topk_w, void* y,
-                                  moe_stream_t stream) {
+                                  const int32_t* row_of, const float* topk_w,
+                                  const void* yshared, void* y, moe_stream_t stream) {
     if (!config_ok(cfg) || T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!yexp || !row_of || !topk_w || !y || !aligned16(yexp) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->has_shared ? (!yshared || !aligned16(yshared)) : (yshared != nullptr))
         return MOE_ERR_INVALID_ARG;
     const moe_config& c = *cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -116,13 +121,13 @@ extern "C" moe_status moe_combine(const moe_config* cfg, int64_t T, const void* 
     const int64_t blocks = ceil_div(T * per, 256);
     const unsigned grid = static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
     if (c.mode == MOE_FP32)
-        combine_f32_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, c.has_shared,
-                                                static_cast<const float*>(yexp), row_of, topk_w,
+        combine_f32_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, static_cast<const float*>(yexp),
+                                                row_of, topk_w, static_cast<const float*>(yshared),
                                                 static_cast<float*>(y));
     else
-        combine_bf16_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, c.has_shared,
-                                                 static_cast<const uint16_t*>(yexp), row_of,
-                                                 topk_w, static_cast<uint16_t*>(y));
+        combine_bf16_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, static_cast<const uint16_t*>(yexp),
+                                                 row_of, topk_w, static_cast<const uint16_t*>(yshared),
+                                                 static_cast<uint16_t*>(y));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -12,7 +12,10 @@
 //   4. gather: each token's quantised row is read once and written to all of its destination
 //      rows (token-major); the scales go, destination-major, to a K-block-major [H/128, R]
 //      array, the layout the grouped GEMM reads.
-// With a shared expert, group E follows with every token once, in order.
+// With a shared expert, group E follows with every token once, in order, from row T*K.
+// An expert id outside [0, E) is dropped: its slot gets row_of = -1 and no row.  The V routed
+// rows then fill [0, V) and the rows [V, T*K) belong to no (token, slot): they get
+// perm_tok = -1, all-zero codes and zero scales, so the GEMMs compute zeros there.
 #include <mutex>
 
 #include "common.cuh"
@@ -51,9 +54,10 @@ constexpr int kScanSlice = 32;  // experts per CTA in the base pass (one per lan
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
             const int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base,
-            int32_t* __restrict__ offs) {
+            int32_t* __restrict__ offs, int32_t* __restrict__ perm_tok) {
     __shared__ int32_t tot[kScanThreads];                  // expert totals, then their starts
     __shared__ int32_t wsum[kScanThreads / 32];
+    __shared__ int32_t n_valid;                            // routed rows claimed by valid ids
     __shared__ int32_t psum[kScanThreads / 32][kScanSlice + 1];  // [part][expert of the slice]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     tot[tid] = 0;
@@ -90,7 +94,12 @@ scan_kernel(int64_t T, int K, int E, int has_shared, int64_t n_chunks,
     }
     __syncthreads();
     tot[tid] = wsum[warp] + incl - x;
+    if (tid == E - 1) n_valid = wsum[warp] + incl;
     __syncthreads();
+    // rows no valid (token, slot) claims: perm_tok = -1 (the scale gather zeroes them)
+    for (int64_t r = n_valid + static_cast<int64_t>(blockIdx.x) * kScanThreads + tid; r < T * K;
+         r += static_cast<int64_t>(gridDim.x) * kScanThreads)
+        perm_tok[r] = -1;
     if (blockIdx.x == 0) {
         if (tid < E) offs[tid] = tot[tid];
         if (tid == 0) {
@@ -163,6 +172,8 @@ positions_match_kernel(int64_t T, int K, int E, int has_shared, const int32_t* _
             const int64_t tt = t0 + i / K;
             perm_tok[pos] = static_cast<int32_t>(tt);
             row_of[t0 * K + i] = pos;
+        } else if (i < n) {
+            row_of[t0 * K + i] = -1;  // dropped slot: no row
         }
     }
     if (has_shared)
@@ -179,7 +190,11 @@ positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restr
     extern __shared__ int32_t sidx[];  // [kChunk * K]
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     const int nt = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
-    for (int i = threadIdx.x; i < nt * K; i += blockDim.x) sidx[i] = idx[t0 * K + i];
+    for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
+        const int32_t e = idx[t0 * K + i];
+        sidx[i] = e;
+        if (e < 0 || e >= E) row_of[t0 * K + i] = -1;  // dropped slot: no row
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int32_t pos = chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
@@ -242,11 +257,14 @@ gather_tokens_kernel(int64_t T, int K, int E, int has_shared, int64_t row_bytes,
 // 32 scale columns the warp reads, row by row, the row's run of scales from its token (one
 // coalesced load of up to 128 bytes per row), transposes the 32 x 32 tile through shared
 // memory, and writes each column's 32 rows as one coalesced store to the K-block-major
-// dst_s[j * R + r].  Rows no valid (token, slot) claimed are not written.
+// dst_s[j * R + r].  A row with perm_tok = -1 (claimed by no (token, slot)) gets zero scales
+// and an all-zero payload row (row_bytes, a multiple of 16); with n_scales = 0 (FP32 rows)
+// only that zeroing runs.
 constexpr int kScaleWarps = 8;
 __global__ void __launch_bounds__(kScaleWarps * 32)
-gather_scales_kernel(int64_t R, int64_t T, int n_scales, const int32_t* __restrict__ perm_tok,
-                     const float* __restrict__ src_s, float* __restrict__ dst_s) {
+gather_scales_kernel(int64_t R, int64_t T, int n_scales, int64_t row_bytes,
+                     const int32_t* __restrict__ perm_tok, const float* __restrict__ src_s,
+                     float* __restrict__ dst_s, uint8_t* __restrict__ dst_rows) {
     __shared__ float tile[kScaleWarps][32][33];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float (*sm)[33] = tile[w];
@@ -254,7 +272,14 @@ gather_scales_kernel(int64_t R, int64_t T, int n_scales, const int32_t* __restri
     for (int64_t gi = static_cast<int64_t>(blockIdx.x) * kScaleWarps + w; gi < n_grp;
          gi += static_cast<int64_t>(gridDim.x) * kScaleWarps) {
         const int64_t r = gi * 32 + lane;
-        int64_t t = r < R ? perm_tok[r] : -1;
+        int64_t t = r < R ? perm_tok[r] : T;
+        uint32_t unclaimed = __ballot_sync(0xffffffffu, t < 0);
+        while (unclaimed) {  // rare: only when the routing held ids outside [0, E)
+            const int i = __ffs(unclaimed) - 1;
+            unclaimed &= unclaimed - 1;
+            uint4* d4 = reinterpret_cast<uint4*>(dst_rows + (gi * 32 + i) * row_bytes);
+            for (int64_t c = lane; c < row_bytes / 16; c += 32) d4[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
         if (t >= T) t = -1;
         for (int j0 = 0; j0 < n_scales; j0 += 32) {
             const int j = j0 + lane;
@@ -264,7 +289,7 @@ gather_scales_kernel(int64_t R, int64_t T, int n_scales, const int32_t* __restri
             }
             __syncwarp();
             const int nj = min(32, n_scales - j0);
-            if (t >= 0)
+            if (r < R)
                 for (int jj = 0; jj < nj; ++jj) dst_s[static_cast<int64_t>(j0 + jj) * R + r] = sm[jj][lane];
             __syncwarp();
         }
@@ -283,7 +308,8 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
                                                                                        chunk_cnt);
     MOE_LAUNCH_CHECK();
     scan_kernel<<<static_cast<unsigned>(ceil_div(E, kScanSlice)), kScanThreads, 0, s>>>(T, K, E, S, n_chunks,
-                                                                                      chunk_cnt, chunk_base, offs);
+                                                                                      chunk_cnt, chunk_base, offs,
+                                                                                      perm_tok);
     MOE_LAUNCH_CHECK();
     const size_t match_smem = sizeof(int32_t) * ceil_div(kChunk * K, 32) * E;
     if (match_smem <= 48 * 1024)
@@ -299,12 +325,11 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
     gather_tokens_kernel<<<static_cast<unsigned>(tok_blocks < 148 * 8 ? tok_blocks : 148 * 8), 256, 0, s>>>(
         T, K, E, S, row_bytes, topk_idx, row_of, static_cast<const uint8_t*>(xq), static_cast<uint8_t*>(aq));
     MOE_LAUNCH_CHECK();
-    if (fp8) {
-        const int64_t blocks = ceil_div(ceil_div(R, 32), kScaleWarps);
-        gather_scales_kernel<<<static_cast<unsigned>(blocks < 148 * 8 ? blocks : 148 * 8), kScaleWarps * 32, 0, s>>>(
-            R, T, c.hidden / 128, perm_tok, xs, as);
-        MOE_LAUNCH_CHECK();
-    }
+    // scales (FP8 mode) and the zeroing of unclaimed rows (both modes)
+    const int64_t blocks = ceil_div(ceil_div(R, 32), kScaleWarps);
+    gather_scales_kernel<<<static_cast<unsigned>(blocks < 148 * 8 ? blocks : 148 * 8), kScaleWarps * 32, 0, s>>>(
+        R, T, fp8 ? c.hidden / 128 : 0, row_bytes, perm_tok, xs, as, static_cast<uint8_t*>(aq));
+    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 

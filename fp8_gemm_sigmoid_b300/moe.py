@@ -52,7 +52,7 @@ _SIGS = {
     "moe_grouped_gemm_fp8": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                              _vp, _sz, _vp],
     "moe_grouped_gemm_f32": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
-    "moe_combine": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp],
+    "moe_combine": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_bias_update": [_cfgp, _i64, _vp, _vp, _vp],
     "moe_forward": [_cfgp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp,
                     _vp, _vp, _sz, _vp],
@@ -168,9 +168,11 @@ def moe_grouped_gemm_f32(n_groups, offs, rows, N, Kdim, A, W, epilogue, out, ws,
         _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def moe_combine(cfg, T, yexp, row_of, topk_w, y, stream=None):
+def moe_combine(cfg, T, yexp, row_of, topk_w, yshared, y, stream=None):
+    """yexp: the routed expert rows [T*K, H] (extra rows after them are ignored); yshared: the
+    shared expert's rows [T, H] (None without a shared expert)."""
     _check("moe_combine", _lib_handle().moe_combine(ctypes.byref(_cfg(cfg)), int(T), _ptr(yexp), _ptr(row_of),
-                                                    _ptr(topk_w), _ptr(y), _stream(stream)))
+                                                    _ptr(topk_w), _ptr(yshared), _ptr(y), _stream(stream)))
 
 
 def moe_bias_update(cfg, T, counts, bias, stream=None):

@@ -143,16 +143,22 @@ MOE_API moe_status moe_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols,
 
 /* a3. [P1] §2.3 token permutation by expert, deterministic: rows are expert-major and,
  * within an expert, in ascending token order (the stable argsort of the flat expert ids).
- * With has_shared, group E follows with every token once, in order.  R = T*K + T*S rows.
- *  topk_idx [T, K] int32 with entries in [0, E) (as moe_gate writes them; an entry outside
- *  that range is dropped and its row is left unwritten); counts [E]: the gate's histogram,
- *  accepted for symmetry and not read (may be NULL) -- the rows are derived from topk_idx;
+ * With has_shared, group E follows with every token once, in order, in rows
+ * [T*K, T*K + T).  R = T*K + T*S rows.
+ *  topk_idx [T, K] int32 with entries in [0, E) (as moe_gate writes them).  An entry outside
+ *  that range is dropped: its row_of entry is -1 and it claims no row.  With V valid entries
+ *  the routed rows fill [0, V); the rows [V, T*K), which the last routed group's range
+ *  [offs[E-1], offs[E]) then also covers, get perm_tok = -1, all-zero codes and zero scales,
+ *  so the grouped GEMMs compute zeros there and moe_combine never reads them.
+ *  counts [E]: the gate's histogram, accepted for symmetry and not read (may be NULL) -- the
+ *  rows are derived from topk_idx;
  *  FP8 mode: xq [T, H] E4M3 and xs [T, H/128] FP32 (from moe_quant_1x128), gathered into
  *            aq [R, H] and as [H/128, R] (K-block-major: as[j * R + r] is the scale of
  *            columns 128j..128j+127 of row r, the layout moe_grouped_gemm_fp8 reads);
  *  FP32 mode: xq is x [T, H] FP32 gathered into aq [R, H] FP32; xs and as are ignored.
- *  Outputs: offs [E + 1 + S] int32 (exclusive prefix sum of the rows per group),
- *  perm_tok [R] int32 (token of each row), row_of [T, K] int32 (row of each (t, k)).
+ *  Outputs: offs [E + 1 + S] int32: offs[e] = rows of the experts before e (e <= E-1),
+ *  offs[E] = T*K, offs[E+1] = T*K + T with the shared expert; perm_tok [R] int32 (token of
+ *  each row, -1 for an unclaimed row), row_of [T, K] int32 (row of each (t, k), -1 if dropped).
  *  ws/ws_bytes: workspace of at least moe_workspace_size(cfg, T) bytes. */
 MOE_API moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
                        const int32_t* counts, const void* xq, const float* xs, int32_t* offs,
@@ -171,7 +177,9 @@ MOE_API moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_t* 
  *    and enqueue nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call before any
- *    stream capture.  MOE_ERR_CUDA if the lookup fails.
+ *    stream capture.  MOE_ERR_CUDA if the lookup fails.  The address is kept for the life of
+ *    the process: after cudaDeviceReset (or any teardown of the device's primary context)
+ *    the kept address is stale, so do not call this entry point on that device again.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *  - Every call shares the array and overwrites it; nothing in it needs to start at zero.
  *    Calls that overlap on the GPU (other streams, other threads) race and must be
@@ -210,14 +218,18 @@ MOE_API moe_status moe_grouped_gemm_f32(int32_t n_groups, const int32_t* offs, i
                                 int32_t epilogue, float* out, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
 
-/* a7. [P1] §2.3 (reverse exchange) / [P2] §3.1 (BF16 combine): for every token t,
- *   y[t] = sum_{k=0..K-1} topk_w[t,k] * yexp[row_of[t,k]] + yexp[T*K + t]  (shared, if S)
+/* a7. [P1] §2.2 (MoEGate weights) and §2.3 (reverse exchange), [P2] §3.1 (BF16 combine):
+ * for every token t,
+ *   y[t] = sum_{k=0..K-1} topk_w[t,k] * yexp[row_of[t,k]] + yshared[t]   (shared, if S)
  * accumulated in FP32 in slot order, shared expert last, rounded once to the output type.
- *  yexp [R, H] BF16 (FP8 mode) or FP32 (FP32 mode); row_of [T, K]; topk_w [T, K];
+ * A slot whose row_of lies outside [0, T*K) (-1: dropped by moe_permute) adds nothing.
+ *  yexp [T*K, H] routed expert rows, BF16 (FP8 mode) or FP32 (FP32 mode); row_of [T, K];
+ *  topk_w [T, K]; yshared [T, H] the shared expert's rows, same type (required when
+ *  has_shared, NULL otherwise; moe_forward passes the rows T*K.. of its expert output);
  *  y [T, H] same type as yexp.  16-byte aligned. */
 MOE_API moe_status moe_combine(const moe_config* cfg, int64_t T, const void* yexp,
-                       const int32_t* row_of, const float* topk_w, void* y,
-                       moe_stream_t stream);
+                       const int32_t* row_of, const float* topk_w, const void* yshared,
+                       void* y, moe_stream_t stream);
 
 /* a8. Load-driven selection-bias update (the bias "adjusted from real-time load" of
  * [P1] §2.2): bias[i] += 1e-3 * sign(T*K/E - counts[i]), with the sign taken in integers
@@ -225,7 +237,10 @@ MOE_API moe_status moe_combine(const moe_config* cfg, int64_t T, const void* yex
 MOE_API moe_status moe_bias_update(const moe_config* cfg, int64_t T, const int32_t* counts,
                            float* bias, moe_stream_t stream);
 
-/* The whole layer forward on one stream: gate (a1), quantisation (a2, FP8 mode),
+/* The whole layer forward ([P1] §2.2 MoEGate and the layer's routed + shared experts;
+ * [P1] §2.3 dispatch and combine, done on one GPU as a permutation and a gather; [P2] §3.1
+ * 8 routed + 1 shared expert per token; [P2] §3.2 the fine-grained FP8 expert GEMMs) on one
+ * stream: gate (a1), quantisation (a2, FP8 mode),
  * permutation (a3), grouped GEMM with SwiGLU (a4), grouped GEMM down-projection (a5), with
  * the shared expert as the last group (a6), combine (a7) and, if update_bias != 0, the bias
  * update (a8) after routing.

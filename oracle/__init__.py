@@ -169,7 +169,9 @@ def gate(x, Wg, bias, n_group, topk_group, top_k, rsf, want_scores=False):
 
 def permute(topk_idx, n_experts, has_shared):
     """[DeepSeek-V3 co-design teardown §2.3] counts and expert-major, token-ascending rows.
-    Returns dict(counts [E], offs [E+1+has_shared], perm_tok [T*K(+T)], row_of [T,K])."""
+    Returns dict(counts [E], offs [E+1+has_shared], perm_tok [T*K(+T)], row_of [T,K]).
+    Ids outside [0, E) are dropped (row_of -1; the rows they leave at the end of the routed
+    part get perm_tok -1), the library's contract for input the gate never produces."""
     topk_idx = _c(topk_idx, np.int32)
     T, K = topk_idx.shape
     E = n_experts
@@ -272,7 +274,7 @@ def _take(W, ids):
     return np.ascontiguousarray(W(ids) if callable(W) else W[ids])
 
 
-def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
+def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None, want_scores=False):
     """The MoE layer forward: gate and permutation over all T tokens, then the expert FFNs
     and the combine for the tokens in `sample` (all tokens when None).  Every output row
     depends only on its own token, so a sample is exact.
@@ -284,12 +286,24 @@ def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     callables ids -> stacked rows.  In fp8 mode `qweights(ids)` may return
     quantize_weights(W13[ids], W2[ids]) from a cache.  Only the experts the sample touches
     are read.  Returns dict with gate outputs, permutation, sample, y (BF16 bits in fp8
-    mode, f32 in fp32 mode), yexp [n, K(+1), H] and, in fp8 mode, the sampled xq/xs."""
+    mode, f32 in fp32 mode), yexp [n, K(+1), H] and, in fp8 mode, the sampled xq/xs; with
+    want_scores, the gate's scores [T,E] too."""
+    g = gate(x, Wg, bias, cfg["n_group"], cfg["topk_group"], cfg["top_k"],
+             cfg["routed_scaling_factor"], want_scores=want_scores)
+    p = permute(g["topk_idx"], cfg["n_experts"], int(bool(cfg["has_shared"])))
+    out = dict(g, **p)
+    out.update(experts_and_combine(cfg, x, g, sample, W13, W2, qweights))
+    return out
+
+
+def experts_and_combine(cfg, x, g, sample, W13, W2, qweights=None):
+    """The second half of forward(): the expert FFNs (routed slots, then the shared expert)
+    and the combine for the tokens in `sample` (all when None), on the routing `g` that
+    gate() returned for the whole batch.  Arguments as for forward(); returns dict(sample,
+    y, yexp and, in fp8 mode, xq/xs of the sampled tokens)."""
     T = x.shape[0]
     E, K = cfg["n_experts"], cfg["top_k"]
     hs = int(bool(cfg["has_shared"]))
-    g = gate(x, Wg, bias, cfg["n_group"], cfg["topk_group"], K, cfg["routed_scaling_factor"])
-    p = permute(g["topk_idx"], E, hs)
     if sample is None:
         sample = np.arange(T, dtype=np.int64)
     sample = np.asarray(sample, dtype=np.int64)
@@ -302,7 +316,7 @@ def forward(cfg, x, Wg, bias, W13, W2, sample=None, qweights=None):
     row_exp = row_exp.ravel()
     needed, local = np.unique(row_exp, return_inverse=True)
     local = local.astype(np.int32)
-    out = dict(g, **p, sample=sample)
+    out = dict(sample=sample)
     if n == 0:
         out.update(y=np.empty((0, x.shape[1]), x.dtype), yexp=None)
         return out

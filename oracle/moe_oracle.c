@@ -378,21 +378,32 @@ void orc_gate(int64_t T, int H, int E, int G, int TG, int K, float rsf,
 
 /* counts[e] = number of (token, slot) pairs routed to e.  Rows are ordered expert-major and,
  * within an expert, by ascending token index (the stable argsort of the flat expert ids).
- * With has_shared, slot group E holds every token once, in order, after the routed rows.
- * offs [E+1+has_shared] is the exclusive prefix sum; perm_tok[row] is the token of a row;
- * row_of[t*K+k] is the row of (t, k). */
+ * With has_shared, slot group E holds every token once, in order, in rows [T*K, T*K + T).
+ * offs [E+1+has_shared]: offs[e] = rows of the experts before e, offs[E] = T*K; perm_tok[row]
+ * is the token of a row; row_of[t*K+k] is the row of (t, k).
+ * An id outside [0, E) never comes out of the gate; the library contract (not the pages)
+ * drops such a slot: it counts for no expert, row_of = -1, and the V valid slots fill rows
+ * [0, V) while rows [V, T*K) get perm_tok = -1 (the last expert's range reaches T*K). */
 void orc_permute(int64_t T, int E, int K, int has_shared, const int32_t* topk_idx,
                  int32_t* counts, int32_t* offs, int32_t* perm_tok, int32_t* row_of)
 {
     int64_t* fill = (int64_t*)calloc((size_t)E, sizeof(int64_t));
     for (int e = 0; e < E; ++e) counts[e] = 0;
-    for (int64_t i = 0; i < T * K; ++i) counts[topk_idx[i]] += 1;
+    for (int64_t i = 0; i < T * K; ++i)
+        if (topk_idx[i] >= 0 && topk_idx[i] < E) counts[topk_idx[i]] += 1;
     offs[0] = 0;
-    for (int e = 0; e < E; ++e) offs[e + 1] = offs[e] + counts[e];
+    for (int e = 1; e < E; ++e) offs[e] = offs[e - 1] + counts[e - 1];
+    int64_t n_valid = (int64_t)offs[E - 1] + counts[E - 1];
+    offs[E] = (int32_t)(T * K);
     if (has_shared) offs[E + 1] = offs[E] + (int32_t)T;
+    for (int64_t r = n_valid; r < T * K; ++r) perm_tok[r] = -1;
     for (int64_t t = 0; t < T; ++t)
         for (int k = 0; k < K; ++k) {
             int e = topk_idx[t * K + k];
+            if (e < 0 || e >= E) {
+                row_of[t * K + k] = -1;
+                continue;
+            }
             int64_t pos = offs[e] + fill[e]++;
             perm_tok[pos] = (int32_t)t;
             row_of[t * K + k] = (int32_t)pos;

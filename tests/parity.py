@@ -4,11 +4,14 @@ Tolerances (written here, used by every parity test):
   - routing indices, per-expert counts, permutation order, quantised codes of the same
     FP32 inputs and the bias update: bit-exact, except on tokens whose selection margin in
     the oracle (k-th vs (k+1)-th selection score, or topk_group-th vs next group score) is
-    below ROUTING_MARGIN -- there the GPU's choice must still be a valid one;
+    below ROUTING_MARGIN -- there the GPU's choice must still be a valid one
+    (check_flagged_routing: a top choice within the margin, with matching weights);
   - routing weights: |gpu - ref| <= WEIGHT_ATOL * routed_scaling_factor (FP32 logits summed in
     another order than the oracle's double sum);
   - layer and expert outputs: max|gpu - ref| / max|ref| <= 5e-3 (FP8 path) or 1e-3 (FP32).
 """
+import itertools
+
 import numpy as np
 import torch
 
@@ -65,6 +68,57 @@ def check_valid_routing(g_idx, n_experts, n_group, topk_group):
     groups = g_idx // (n_experts // n_group)
     for row in groups:
         assert len(set(row.tolist())) <= topk_group
+
+
+def _top2_group_scores(c, n_group):
+    """Group score of [DeepSeek-V3 co-design teardown §2.2]: the sum of the two largest
+    selection scores of each group (float32, larger first)."""
+    g = np.sort(c.reshape(n_group, -1), axis=1)[:, ::-1]
+    return (g[:, 0] + g[:, 1]).astype(np.float32)
+
+
+def check_flagged_routing(g_idx, g_w, ref, bias, n_group, topk_group, rsf, tol=ROUTING_MARGIN):
+    """On the tokens the oracle flags (selection margin below tol), where several choices are
+    correct up to the rounding of the scores, the GPU's choice must be one of them.  With the
+    oracle's scores s (ref["scores"]) and selection scores c = s + bias:
+      - the GPU's experts lie in a set S of topk_group groups that is a top-topk_group choice
+        by group score within tol (every group of S at least the cut - tol, every other group
+        at most the lowest of S + tol);
+      - their summed selection score is within top_k * tol of the best top_k sum inside S;
+      - the weight paired with each chosen expert is its score normalised over the chosen set
+        (top_k > 1) times rsf, within WEIGHT_ATOL * rsf.
+    Returns the number of tokens checked."""
+    flagged = np.nonzero(ref["margin"] < tol)[0]
+    if flagged.size == 0:
+        return 0
+    assert "scores" in ref, "the oracle's scores are needed to validate flagged tokens"
+    T, K = g_idx.shape
+    E = ref["scores"].shape[1]
+    gsz = E // n_group
+    for t in flagged:
+        s = ref["scores"][t].astype(np.float32)
+        c = (s + bias).astype(np.float32)
+        gs = _top2_group_scores(c, n_group)
+        cut = np.sort(gs)[::-1][topk_group - 1]
+        used = set((g_idx[t] // gsz).tolist())
+        ok = False
+        for S in itertools.combinations(range(n_group), topk_group):
+            if not used <= set(S):
+                continue
+            lo = min(gs[g] for g in S)
+            if lo < cut - tol or any(gs[g] > lo + tol for g in range(n_group) if g not in S):
+                continue
+            allowed = np.array([e for e in range(E) if e // gsz in S])
+            best = np.sort(c[allowed].astype(np.float64))[::-1][:K].sum()
+            if c[g_idx[t]].astype(np.float64).sum() >= best - K * tol:
+                ok = True
+                break
+        assert ok, "token %d: the GPU's experts %s are not a valid choice" % (t, g_idx[t].tolist())
+        sel = s[g_idx[t]].astype(np.float64)
+        want = sel / (sel.sum() + 1e-20) * rsf if K > 1 else sel * rsf
+        err = np.max(np.abs(g_w[t] - want))
+        assert err <= WEIGHT_ATOL * rsf, "token %d: weights differ by %g" % (t, err)
+    return int(flagged.size)
 
 
 def check_permutation(p_gpu, idx, orc, n_experts, has_shared):

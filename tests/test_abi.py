@@ -166,10 +166,15 @@ def test_more_host_side_rejections(moe):
     assert L.moe_gate(c, 8, vp(16), vp(16), vp(16), vp(16), vp(16), None, None) == INV
     assert L.moe_gate(cb, 8, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
     assert L.moe_gate(c, 8, None, vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
-    # combine: T == 0 enqueues nothing and succeeds; missing or misaligned buffers are refused
-    assert L.moe_combine(c, 0, None, None, None, None, None) == moe.MOE_OK
-    assert L.moe_combine(c, 8, None, vp(16), vp(16), vp(16), None) == INV
-    assert L.moe_combine(c, 8, vp(16), vp(16), vp(16), vp(24), None) == INV
+    # combine: T == 0 enqueues nothing and succeeds; missing or misaligned buffers are refused;
+    # the shared expert's rows are required exactly when the layer has a shared expert
+    assert L.moe_combine(c, 0, None, None, None, None, None, None) == moe.MOE_OK
+    assert L.moe_combine(c, 8, None, vp(16), vp(16), vp(16), vp(16), None) == INV
+    assert L.moe_combine(c, 8, vp(16), vp(16), vp(16), vp(16), vp(24), None) == INV
+    assert L.moe_combine(c, 8, vp(16), vp(16), vp(16), None, vp(16), None) == INV
+    assert L.moe_combine(c, 8, vp(16), vp(16), vp(16), vp(24), vp(16), None) == INV
+    no_shared = moe.make_config(dict(sy.config("v3_prefill"), has_shared=0))
+    assert L.moe_combine(ctypes.byref(no_shared), 8, vp(16), vp(16), vp(16), vp(16), vp(16), None) == INV
     # bias update
     assert L.moe_bias_update(c, 8, vp(16), None, None) == INV
     assert L.moe_bias_update(c, -1, vp(16), vp(16), None) == INV

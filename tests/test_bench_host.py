@@ -35,24 +35,36 @@ def _sha(stage):
 
 
 def test_measured_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch):
+    # a capture on a cut-down case (T=2048, 32 experts: the same rows per expert) scales to the
+    # full workload by the tokens processed
     f = tmp_path / "traffic.txt"
-    f.write_text("# workload stage sha read write\n"
-                 "v3_prefill gate %s 1000 24\n"
-                 "v3_prefill combine %s 7 8\n" % (_sha("gate"), "0" * 64))
+    f.write_text("# workload stage sha read write T E\n"
+                 "v3_prefill gate %s 1000 24 2048 32\n"
+                 "v3_prefill combine %s 7 8 2048 32\n"
+                 "v3_prefill quant %s 7 8 2048 64\n" % (_sha("gate"), "0" * 64, _sha("quant")))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.measured_traffic("gate", "v3_prefill") == 1024
-    assert bench.measured_traffic("combine", "v3_prefill") is None  # source changed since
-    assert bench.measured_traffic("gate", "v3_decode") is None       # other workload
-    assert bench.measured_traffic("bias_update", "v3_prefill") is None
+    full = sy.config("v3_prefill")
+    assert bench.measured_traffic("gate", full)[0] == 1024 * 8
+    assert bench.measured_traffic("gate", sy.config("v3_prefill", T=2048, n_experts=32))[0] == 1024
+    assert bench.measured_traffic("combine", full) == (None, None)   # source changed since
+    assert bench.measured_traffic("quant", full) == (None, None)     # another rows-per-expert shape
+    assert bench.measured_traffic("gate", sy.config("v3_decode")) == (None, None)  # other workload
+    assert bench.measured_traffic("bias_update", full) == (None, None)
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
-    assert bench.measured_traffic("gate", "v3_prefill") is None
+    assert bench.measured_traffic("gate", full) == (None, None)
 
 
 def test_recorded_traffic_file_is_well_formed():
     with open(bench.TRAFFIC_FILE) as f:
         rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
-    assert rows
-    for workload, stage, sha, rd, wr in rows:
+    for workload, stage, sha, rd, wr, cap_T, cap_E in rows:
         assert workload in sy.CONFIGS and stage in bench.KERNEL_SOURCES
         assert len(sha) == 64 and int(sha, 16) >= 0
-        assert int(rd) > 0 and int(wr) >= 0
+        assert int(rd) > 0 and int(wr) >= 0 and int(cap_T) > 0 and int(cap_E) > 0
+
+
+def test_gemm_rows_counts_whole_tiles():
+    r = bench.gemm_rows([0, 1, 128, 129, 256], T=300, has_shared=1)
+    assert r["useful"] == 0 + 1 + 128 + 129 + 256 + 300
+    assert r["tile_rows"] == (0 + 1 + 1 + 2 + 2 + 3) * 128
+    assert r["tile_efficiency"] == r["useful"] / r["tile_rows"]

@@ -252,6 +252,46 @@ def test_gate_ties_go_to_lower_index(orc):
     assert np.all(g["margin"] == 0)
 
 
+def _margin_case(orc, bias_units, G, TG, K):
+    """Zero logits give every score exactly 1/2, so the selection scores are 1/2 + b; with b
+    a multiple of u = 2^-20 every selection score, group score and margin below is exact."""
+    E = len(bias_units)
+    u = 2.0 ** -20
+    b = (np.asarray(bias_units, np.float64) * u).astype(np.float32)
+    x = np.zeros((2, 32), np.float32)
+    Wg = np.zeros((E, 32), np.float32)
+    return orc.gate(x, Wg, b, G, TG, K, 1.0), u
+
+
+def test_gate_margin_is_the_smaller_of_the_two_cuts(orc):
+    # groups of 4; the margin is min(TG-th kept group score - best dropped group score,
+    # K-th chosen selection score - best unchosen candidate in the kept groups)
+    # group scores (top-2 sums, in units over 1): g0 19, g1 14, g2 13, g3 0 -> group cut 1
+    # kept experts by score: 10, 9, 8, then 6 -> expert cut (K = 3) 2
+    g, u = _margin_case(orc, [10, 9, 0, 0, 8, 6, 0, 0, 7, 6, 0, 0, 0, 0, 0, 0], 4, 2, 3)
+    assert g["topk_idx"][0].tolist() == [0, 1, 4]
+    assert np.all(g["margin"] == np.float32(u))
+    # a wider group cut (g2 9): now the expert cut, 2 units, is the smaller
+    g, u = _margin_case(orc, [10, 9, 0, 0, 8, 6, 0, 0, 5, 4, 0, 0, 0, 0, 0, 0], 4, 2, 3)
+    assert np.all(g["margin"] == np.float32(2 * u))
+    # every group kept: no group cut, the expert cut alone (top-4: 10 9 8 7, next 6 -> 1)
+    g, u = _margin_case(orc, [10, 9, 0, 0, 8, 6, 0, 0, 7, 3, 0, 0, 0, 0, 0, 0], 4, 4, 4)
+    assert g["topk_idx"][0].tolist() == [0, 1, 4, 8]
+    assert np.all(g["margin"] == np.float32(u))
+    # K takes every expert of the kept groups: no expert cut, the group cut alone (19 - 14 = 5)
+    g, u = _margin_case(orc, [10, 9, 1, 0, 8, 6, 0, 0, 7, 7, 0, 0, 0, 0, 0, 0], 4, 1, 4)
+    assert sorted(g["topk_idx"][0].tolist()) == [0, 1, 2, 3]
+    assert np.all(g["margin"] == np.float32(5 * u))
+    # an exact tie at the expert cut (8 and 8) gives margin 0; the lower index is chosen
+    g, u = _margin_case(orc, [10, 9, 0, 0, 8, 0, 0, 0, 8, 6, 0, 0, 0, 0, 0, 0], 4, 3, 3)
+    assert g["topk_idx"][0].tolist() == [0, 1, 4]
+    assert np.all(g["margin"] == 0)
+    # an exact tie at the group cut (14 and 14, top-1 group... g1 and g2 tie for the 2nd)
+    g, u = _margin_case(orc, [10, 9, 0, 0, 8, 6, 0, 0, 7, 7, 0, 0, 0, 0, 0, 0], 4, 2, 2)
+    assert g["topk_idx"][0].tolist() == [0, 1]
+    assert np.all(g["margin"] == 0)
+
+
 def test_gate_masked_experts_never_chosen_even_with_negative_scores(orc):
     # every selection score negative: the kept groups still bound the choice
     rng = np.random.default_rng(6)
@@ -335,6 +375,39 @@ def test_permute_empty_and_full_experts(orc):
     assert p["offs"].tolist() == [0, 0, 0, T, T, T, T, 2 * T, 2 * T]
     assert np.array_equal(p["row_of"][:, 0], np.arange(T) + T)
     assert np.array_equal(p["row_of"][:, 1], np.arange(T))
+
+
+def test_permute_drops_ids_outside_range(orc):
+    # the library's contract for ids the gate never produces: such a slot counts for no
+    # expert and gets no row (row_of -1); the valid slots keep the stable expert-major order
+    # in rows [0, V) and the rows [V, T*K) are unclaimed (perm_tok -1), the shared group
+    # still starting at T*K
+    rng = np.random.default_rng(21)
+    T, E, K = 97, 12, 3
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[4, 1] = -1
+    idx[10, 0] = E
+    idx[50, 2] = 1 << 20
+    idx[96] = [-5, -6, -7]
+    for has_shared in (0, 1):
+        p = orc.permute(idx, E, has_shared)
+        flat = idx.ravel()
+        ok = (flat >= 0) & (flat < E)
+        V = int(ok.sum())
+        pos = np.nonzero(ok)[0]
+        order = pos[np.argsort(flat[ok], kind="stable")]
+        assert np.array_equal(p["perm_tok"][:V], order // K)
+        assert np.all(p["perm_tok"][V:T * K] == -1)
+        assert np.array_equal(p["counts"], np.bincount(flat[ok], minlength=E))
+        assert np.array_equal(p["offs"][:E], np.concatenate([[0], np.cumsum(p["counts"])[:-1]]))
+        assert p["offs"][E] == T * K
+        rows = p["row_of"].ravel()
+        assert np.all(rows[~ok] == -1)
+        assert np.array_equal(np.sort(rows[ok]), np.arange(V))
+        assert np.array_equal(p["perm_tok"][rows[ok]], pos // K)
+        if has_shared:
+            assert p["offs"][E + 1] == T * K + T
+            assert np.array_equal(p["perm_tok"][T * K:], np.arange(T))
 
 
 def test_bias_update_hand_examples(orc):
