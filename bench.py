@@ -25,7 +25,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from fp8_gemm_sigmoid_b300 import moe, synthetic as sy  # noqa: E402
+from fp8_gemm_sigmoid_b300 import moe, replicas, synthetic as sy  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -186,14 +186,22 @@ class Layer:
         self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)  # K-block-major
         self.yexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
 
-    def forward(self):
+    def forward(self, world=1):
+        """One layer step.  Under N > 1 token replicas the top-1 bias update runs after an
+        all-reduce of the histogram, so every rank updates from the whole batch's load."""
         o = self.out
-        moe.moe_forward(self.cfg, self.x, self.weights, self.bias, self.cfg["update_bias"], self.y,
+        replicated = world > 1 and self.cfg["update_bias"]
+        moe.moe_forward(self.cfg, self.x, self.weights, self.bias,
+                        0 if replicated else self.cfg["update_bias"], self.y,
                         o["topk_idx"], o["topk_w"], o["counts"], self.ws)
+        if replicated:
+            replicas.global_bias_update(self.cfg, o["counts"], self.cfg["T"], self.bias,
+                                        lambda c, Tg, cnt, b: moe.moe_bias_update(c, Tg, cnt, b),
+                                        T_global=world * self.cfg["T"])
 
     STAGES = ["gate", "quant", "permute", "gemm1_swiglu", "gemm2_down", "combine", "bias_update"]
 
-    def staged(self, ev):
+    def staged(self, ev, world=1):
         """The same layer through the individual entry points, an event after each stage."""
         c, o = self.cfg, self.out
         T, H, I, E = c["T"], c["hidden"], c["inter"], c["n_experts"]
@@ -216,7 +224,12 @@ class Layer:
         moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], ysh, self.y)
         ev[6].record()
         if c["update_bias"]:
-            moe.moe_bias_update(c, T, o["counts"], self.bias)
+            if world > 1:  # token replicas: the update from the whole batch's histogram
+                replicas.global_bias_update(c, o["counts"], T, self.bias,
+                                            lambda cc, Tg, cnt, b: moe.moe_bias_update(cc, Tg, cnt, b),
+                                            T_global=world * T)
+            else:
+                moe.moe_bias_update(c, T, o["counts"], self.bias)
         ev[7].record()
 
     def launches_per_step(self):
@@ -361,7 +374,7 @@ def cpu_baseline(cfg, layer, n_sample):
     return {"value": value, "unit": "tokens/s", "cores": ol.oracle.num_threads(), "kind": "oracle",
             "sample": "gate + permutation over all %d tokens (%.2f s), expert FFNs + combine on a seeded "
                       "%d-token sample (%.2f s), extrapolated per token to %d tokens"
-                      % (T, t_gate, n, t_exp, T, T)}
+                      % (T, t_gate, n, t_exp, T)}
 
 
 def run_reference(args, cfg, rank, world):
@@ -510,10 +523,10 @@ def main():
 
     # warm-up (W whole-layer steps through moe_forward and through the staged calls)
     for _ in range(max(args.warmup, 3)):
-        layer.forward()
+        layer.forward(world)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
     for _ in range(2):
-        layer.staged(ev)
+        layer.staged(ev, world)
     barrier_sync(dist_on)
 
     # timed region 1: K steps of moe_forward (the headline)
@@ -523,7 +536,7 @@ def main():
     r1 = [clocks.now()]
     start.record(stream)
     for _ in range(args.steps):
-        layer.forward()
+        layer.forward(world)
     stop.record(stream)
     barrier_sync(dist_on)
     r1.append(clocks.now())
@@ -542,7 +555,7 @@ def main():
     all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_staged)]
     r2 = [clocks.now()]
     for evs in all_evs:
-        layer.staged(evs)
+        layer.staged(evs, world)
     barrier_sync(dist_on)
     r2.append(clocks.now())
     for evs in all_evs:
