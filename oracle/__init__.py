@@ -47,6 +47,8 @@ def lib():
         L.orc_ffn_fp8_pow2.argtypes = L.orc_ffn_fp8.argtypes
         L.orc_ffn_f32.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp]
         L.orc_combine.argtypes = [i64, i32, i32, vp, vp, i32, vp, vp]
+        L.orc_logfmt_encode.argtypes = [i64, i64, vp, i32, i32, vp, vp, vp, vp]
+        L.orc_logfmt_decode.argtypes = [i64, i64, vp, i32, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -338,4 +340,35 @@ def experts_and_combine(cfg, x, g, sample, W13, W2, qweights=None):
         acc = combine(yrows[:, :K], g["topk_w"][sample],
                       np.ascontiguousarray(yrows[:, K]) if hs else None)
         out.update(y=acc, yexp=yrows)
+    return out
+
+
+# ---------------------------------------------------------------- LogFMT codec
+
+def logfmt_encode(x, n_bits):
+    """[Insights into DeepSeek-V3 précis §3.2, LogFMT-nBit] per 1x128 tile: min and max of the
+    natural log of the non-zero magnitudes (min held above max - ln 2^32), Step = (max - min) /
+    (2^(n-1) - 2), each value coded with the K whose exp(min + Step (K-1)) is nearest in linear
+    space (K = 0: zero), sign in the top bit.  x [rows, cols] float32 or BF16 bits.
+    Returns dict(codes uint16 [rows, cols], lmin f32 [rows, cols/128], step f32 [...],
+    margin f32 [rows, cols]: distance to the decision midpoint as a fraction of the gap)."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 128 == 0 and 3 <= n_bits <= 16
+    codes = np.empty((rows, cols), np.uint16)
+    lmin = np.empty((rows, cols // 128), np.float32)
+    step = np.empty((rows, cols // 128), np.float32)
+    margin = np.empty((rows, cols), np.float32)
+    lib().orc_logfmt_encode(rows, cols, _p(x), _is_bf16(x), int(n_bits), _p(codes), _p(lmin), _p(step),
+                            _p(margin))
+    return dict(codes=codes, lmin=lmin, step=step, margin=margin)
+
+
+def logfmt_decode(codes, lmin, step, n_bits):
+    """Inverse of logfmt_encode: +-exp(min + Step (K-1)) (0 for K = 0), float32 [rows, cols]."""
+    codes = _c(codes, np.uint16)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols), np.float32)
+    lib().orc_logfmt_decode(rows, cols, _p(codes), int(n_bits), _p(_c(lmin, np.float32)),
+                            _p(_c(step, np.float32)), _p(out))
     return out

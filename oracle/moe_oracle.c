@@ -578,3 +578,100 @@ void orc_combine(int64_t n_tok, int K, int H, const void* yk, const void* ysh, i
         }
     }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* [P2 §3.2] LogFMT-nBit: a logarithmic code for 1x128 tiles of the combine payload      */
+/* ------------------------------------------------------------------------------------ */
+
+/* The précis' description (Insights into DeepSeek-V3 §3.2, LogFMT communication compression):
+ * per 1x128 tile take the logarithm of the magnitudes and their min and max; the min is coded
+ * S.00..01 and the max S.11..11, Step = (max - min) / (2^(n-1) - 2), zero is S.00..00, every
+ * other value is rounded to an integer multiple K of Step, and K decodes to
+ * exp(min + Step * (K - 1)); the rounding must happen in linear space (unbiased), and min is
+ * held above max - ln(2^32).  Readings where the text is silent:
+ *  - natural logarithm (the decoder is written with exp);
+ *  - min and max run over the tile's non-zero values; a tile of zeros has min = Step = 0 and
+ *    all codes zero; a tile whose non-zero magnitudes are all equal has Step = 0 and codes 1;
+ *  - the tile's metadata travel as two FP32 numbers (min, Step), and the grid the decoder
+ *    rebuilds from them, d(K) = exp(min + Step * (K - 1)), is the grid the encoder rounds to;
+ *  - "rounding in linear space": a magnitude a is coded with the K whose d(K) is nearest to a
+ *    (with d(0) = 0), ties to the larger K; K never exceeds 2^(n-1) - 1;
+ *  - the sign is the top bit of the n-bit code (S), also for zero.
+ * Decisions are taken in double on the FP32 metadata.  margin_out (may be NULL) receives, per
+ * value, its distance to the decision midpoint as a fraction of the gap between the two
+ * neighbouring grid values (+inf where no choice was made). */
+static double logfmt_grid(double lmin, double step, int K)
+{
+    return K == 0 ? 0.0 : exp(lmin + step * (double)(K - 1));
+}
+
+void orc_logfmt_encode(int64_t rows, int64_t cols, const void* x, int x_is_bf16, int n_bits,
+                       uint16_t* codes, float* lmin_out, float* step_out, float* margin_out)
+{
+    const int kmax = (1 << (n_bits - 1)) - 1;
+    const int64_t tiles = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t tt = 0; tt < rows * tiles; ++tt) {
+        const int64_t base = (tt / tiles) * cols + (tt % tiles) * 128;
+        double amax = 0.0, amin = INFINITY;
+        for (int j = 0; j < 128; ++j) {
+            double a = fabs((double)load_elem(x, x_is_bf16, base + j));
+            if (a > 0.0) {
+                if (a > amax) amax = a;
+                if (a < amin) amin = a;
+            }
+        }
+        float lmin_f = 0.0f, step_f = 0.0f;
+        if (amax > 0.0) {
+            double lmax = log(amax), lmn = log(amin);
+            if (lmn < lmax - 32.0 * log(2.0)) lmn = lmax - 32.0 * log(2.0);
+            lmin_f = (float)lmn;
+            step_f = (float)((lmax - lmn) / (double)(kmax - 1));
+        }
+        lmin_out[tt] = lmin_f;
+        step_out[tt] = step_f;
+        for (int j = 0; j < 128; ++j) {
+            float v = load_elem(x, x_is_bf16, base + j);
+            uint16_t sgn = signbit(v) ? (uint16_t)(1u << (n_bits - 1)) : 0;
+            double a = fabs((double)v);
+            int K = 0;
+            double mg = INFINITY;
+            if (a > 0.0) {
+                if (step_f == 0.0f) {
+                    K = 1;
+                } else {
+                    double r = (log(a) - (double)lmin_f) / (double)step_f + 1.0;
+                    int k0 = r < 0.0 ? 0 : (r > (double)kmax ? kmax : (int)floor(r));
+                    if (k0 >= kmax) {
+                        K = kmax;
+                    } else {
+                        double lo = logfmt_grid(lmin_f, step_f, k0), hi = logfmt_grid(lmin_f, step_f, k0 + 1);
+                        double mid = 0.5 * (lo + hi);
+                        K = a >= mid ? k0 + 1 : k0;
+                        mg = fabs(a - mid) / (hi - lo);
+                    }
+                }
+            }
+            codes[base + j] = sgn | (uint16_t)K;
+            if (margin_out) margin_out[base + j] = (float)mg;
+        }
+    }
+}
+
+/* Decode: K = code & (2^(n-1) - 1); value = +-exp(min + Step * (K - 1)) for K >= 1, +-0 for
+ * K = 0, in double, rounded to FP32. */
+void orc_logfmt_decode(int64_t rows, int64_t cols, const uint16_t* codes, int n_bits,
+                       const float* lmin, const float* step, float* out)
+{
+    const int kmask = (1 << (n_bits - 1)) - 1;
+    const int64_t tiles = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t tt = 0; tt < rows * tiles; ++tt) {
+        const int64_t base = (tt / tiles) * cols + (tt % tiles) * 128;
+        for (int j = 0; j < 128; ++j) {
+            uint16_t c = codes[base + j];
+            double m = logfmt_grid(lmin[tt], step[tt], c & kmask);
+            out[base + j] = (float)((c >> (n_bits - 1)) & 1 ? -m : m);
+        }
+    }
+}
