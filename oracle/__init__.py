@@ -302,7 +302,8 @@ def experts_and_combine(cfg, x, g, sample, W13, W2, qweights=None):
     """The second half of forward(): the expert FFNs (routed slots, then the shared expert)
     and the combine for the tokens in `sample` (all when None), on the routing `g` that
     gate() returned for the whole batch.  Arguments as for forward(); returns dict(sample,
-    y, yexp and, in fp8 mode, xq/xs of the sampled tokens)."""
+    y, yexp and, in fp8 mode, xq/xs of the sampled tokens and y_f32, the FP32 sums that y
+    rounds to BF16)."""
     T = x.shape[0]
     E, K = cfg["n_experts"], cfg["top_k"]
     hs = int(bool(cfg["has_shared"]))
@@ -333,7 +334,7 @@ def experts_and_combine(cfg, x, g, sample, W13, W2, qweights=None):
         yrows = ffn_fp8(xq[rep], xs[rep], local, *qw, pow2=pow2).reshape(n, K + hs, -1)
         acc = combine(yrows[:, :K], g["topk_w"][sample],
                       np.ascontiguousarray(yrows[:, K]) if hs else None)
-        out.update(y=round_bf16(acc), yexp=yrows, xq=xq, xs=xs)
+        out.update(y=round_bf16(acc), y_f32=acc, yexp=yrows, xq=xq, xs=xs)
     else:
         xr = np.ascontiguousarray(np.repeat(x[sample], K + hs, axis=0))
         yrows = ffn_f32(xr, local, _take(W13, needed), _take(W2, needed)).reshape(n, K + hs, -1)
