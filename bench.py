@@ -598,6 +598,33 @@ def main():
                "api": "moe_pipeline_submit (pinned host buffers)"}
         del pl
         torch.cuda.empty_cache()
+    # the LogFMT-8 codec on the combine payload (the routed expert rows, BF16): encode and
+    # decode timed apart from the layer step, each K calls between events
+    logfmt = None
+    if cfg["mode"] == "fp8":
+        payload = layer.yexp[:T * cfg["top_k"]].view(torch.uint16)
+        rows_l, cols_l = payload.shape
+        codes = torch.empty(rows_l, cols_l, dtype=torch.uint8, device=dev)
+        lmin = torch.empty(rows_l, cols_l // 128, dtype=torch.float32, device=dev)
+        lstep = torch.empty_like(lmin)
+        back = torch.empty_like(payload)
+        logfmt = {"n_bits": 8, "rows": rows_l, "cols": cols_l}
+        for name, fn, nbytes in (
+                ("encode", lambda: moe.moe_logfmt_encode(8, payload, codes, lmin, lstep),
+                 rows_l * cols_l * 3 + lmin.numel() * 8),
+                ("decode", lambda: moe.moe_logfmt_decode(8, codes, lmin, lstep, back),
+                 rows_l * cols_l * 3 + lmin.numel() * 8)):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t_ms = a.elapsed_time(b) / args.steps
+            logfmt[name] = {"ms": t_ms, "GB/s": nbytes / t_ms / 1e6, "frac_hbm": nbytes / t_ms / 1e6 / peaks["hbm"]}
+        del codes, lmin, lstep, back
     clocks.stop()
     clk = clocks.stats(*r1)
     stage_clk = clocks.stats(*r2)
@@ -658,6 +685,7 @@ def main():
                          "rows": gemm_rows(counts, T, cfg["has_shared"])},
         "stages": stages,
         "staged_steps": n_staged,
+        "logfmt": logfmt,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -1,0 +1,216 @@
+// logfmt.cu -- LogFMT-nBit, the logarithmic code for 1x128 tiles of the combine payload
+// (Insights into DeepSeek-V3 précis §3.2, LogFMT communication compression): per tile the
+// natural logs of the non-zero magnitudes give min and max (min held above max - ln 2^32),
+// Step = (max - min) / (2^(n-1) - 2); a value is coded with the K >= 1 whose
+// exp(min + Step (K - 1)) is nearest to it in linear space (K = 0: nearer to zero than to
+// exp(min)); the sign is the code's top bit.  Tile metadata: min and Step as FP32.
+//
+// Encoding decides K with one base-2 logarithm per value, relative to the tile's first grid
+// point g1 = e^min: with r = log2(a / g1) / Step2 (Step2 = Step / ln 2) the value lies between
+// the grid points floor(r) + 1 and floor(r) + 2, and the linear midpoint of two neighbours is
+// at the fraction theta = log2((1 + 2^Step2) / 2) / Step2 of the way between them in log
+// space (the same for every pair of the tile), so K = floor(r) + 1 + (frac(r) >= theta);
+// below g1 the midpoint with zero is at r = -1 / Step2.  Logarithms are taken as the
+// exponent plus log2 of the significand in [1, 2) (hardware approximation, absolute error
+// near 2^-22), so r is within about 1e-4 of a step for n <= 12 (the step shrinks as
+// 2^-(n-1)).  Decoding forms 2^(Step2 (K - 1)) from an exactly split exponent (integer part,
+// fraction, and the FMA residual of the product), times g1 = e^min computed once per tile,
+// a few 1e-7 off the exact value before its rounding to BF16.
+// One warp per tile, 4 values per lane (an 8-byte BF16 load); HBM-bound: 2 bytes read and
+// 1 (n <= 8) or 2 bytes written per value.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.442695040888963407f;
+constexpr float kLog2eLo = 1.925963033500011e-08f;  // log2(e) - kLog2e
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x) for finite x > 0 (subnormals included): exponent + log2(significand in [1, 2)).
+__device__ __forceinline__ float log2_split(float x) {
+    int bias = 127;
+    if (x < 1.17549435e-38f) {  // subnormal: scale into the normal range first
+        x *= 18446744073709551616.f;  // 2^64
+        bias += 64;
+    }
+    const uint32_t u = __float_as_uint(x);
+    const int e = static_cast<int>((u >> 23) & 0xffu) - bias;
+    const float m = __uint_as_float((u & 0x007fffffu) | 0x3f800000u);
+    return static_cast<float>(e) + __log2f(m);
+}
+
+template <typename CodeT>
+__global__ void __launch_bounds__(256)
+logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n_bits,
+                     const uint2* __restrict__ x, CodeT* __restrict__ codes,
+                     float* __restrict__ lmin_out, float* __restrict__ step_out) {
+    const int lane = threadIdx.x & 31;
+    const int kmax = (1 << (n_bits - 1)) - 1;
+    const uint32_t sign_bit = 1u << (n_bits - 1);
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tiles;
+         t += nwarps) {
+        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
+        const uint2 raw = x[base / 4];
+        float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
+        float amax = 0.f, amin = INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = fabsf(v[i]);
+            amax = fmaxf(amax, a);
+            if (a > 0.f) amin = fminf(amin, a);
+        }
+        amax = warp_max(amax);
+        amin = warp_min(amin);
+        float step2 = 0.f, l2min = 0.f;
+        if (amax > 0.f) {
+            const float l2max = log2_split(amax);
+            const float span2 = fminf(l2max - log2_split(amin), 32.f);  // max - min held <= log2 2^32
+            l2min = l2max - span2;
+            step2 = __fdividef(span2, static_cast<float>(kmax - 1));
+        }
+        uint32_t c[4];
+        if (step2 > 0.f) {
+            const float inv = __fdividef(1.f, step2);
+            const float theta = log2_split(0.5f + 0.5f * ex2_approx(step2)) * inv;  // linear midpoint, in steps
+            const float zero_cut = -inv;
+            // 1 / g1, unless g1 lies so low (tiles of subnormal BF16 values) that 1 / g1 would
+            // overflow; then the logarithm is taken first and g1's subtracted (a rare, slower
+            // and slightly less precise path)
+            const bool tiny = l2min < -100.f;
+            const float anchor = tiny ? 1.f : ex2_approx(-l2min);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a = fabsf(v[i]);
+                int K = 0;
+                if (a > 0.f) {
+                    const float r = (tiny ? log2_split(a) - l2min : log2_split(a * anchor)) * inv;  // 0 at g1
+                    if (r < 0.f) {
+                        K = r >= zero_cut ? 1 : 0;
+                    } else {
+                        const float fl = floorf(r);
+                        K = static_cast<int>(fl) + 1 + (r - fl >= theta ? 1 : 0);
+                        K = K > kmax ? kmax : K;
+                    }
+                }
+                c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
+            }
+        } else {  // all zero (K = 0), or one magnitude (K = 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                c[i] = (fabsf(v[i]) > 0.f ? 1u : 0u) | (signbit(v[i]) ? sign_bit : 0u);
+        }
+        if (sizeof(CodeT) == 1) {
+            *reinterpret_cast<uint32_t*>(codes + base) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+        } else {
+            *reinterpret_cast<uint2*>(codes + base) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        }
+        if (lane == 0) {
+            lmin_out[t] = l2min * kLn2;
+            step_out[t] = step2 * kLn2;
+        }
+    }
+}
+
+template <typename CodeT>
+__global__ void __launch_bounds__(256)
+logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n_bits,
+                     const CodeT* __restrict__ codes, const float* __restrict__ lmin,
+                     const float* __restrict__ step, uint2* __restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t kmask = (1u << (n_bits - 1)) - 1u;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tiles;
+         t += nwarps) {
+        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
+        uint32_t c[4];
+        if (sizeof(CodeT) == 1) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + base);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] = (w >> (8 * i)) & 0xffu;
+        } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(codes + base);
+            c[0] = w.x & 0xffffu; c[1] = w.x >> 16; c[2] = w.y & 0xffffu; c[3] = w.y >> 16;
+        }
+        // g1 = e^min once per tile; Step2 = Step * log2(e) as an exact pair (hi + lo)
+        const float st = step[t];
+        const float g1 = expf(lmin[t]);
+        const float s_hi = st * kLog2e;
+        const float s_lo = fmaf(st, kLog2e, -s_hi) + st * kLog2eLo;
+        uint16_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t K = c[i] & kmask;
+            float m = 0.f;
+            if (K) {
+                const float k = static_cast<float>(K - 1);
+                const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
+                const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
+                const float ip = floorf(e_hi);
+                const float f = ex2_approx(e_hi - ip) * fmaf(e_lo, kLn2, 1.f);
+                m = ldexpf(g1 * f, static_cast<int>(ip));
+            }
+            o[i] = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
+        }
+        y[base / 4] = make_uint2(o[0] | (static_cast<uint32_t>(o[1]) << 16), o[2] | (static_cast<uint32_t>(o[3]) << 16));
+    }
+}
+
+unsigned warp_grid(int64_t n_tiles) {
+    const int64_t blocks = ceil_div(n_tiles, 8);
+    return static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_logfmt_encode(int32_t n_bits, int64_t rows, int64_t cols, const uint16_t* x,
+                                        void* codes, float* lmin, float* step, moe_stream_t stream) {
+    if (n_bits < 3 || n_bits > 12 || rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!x || !codes || !lmin || !step || !aligned16(x) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+    const int64_t tpr = cols / 128, n_tiles = rows * tpr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_bits <= 8)
+        logfmt_encode_kernel<uint8_t><<<warp_grid(n_tiles), 256, 0, s>>>(
+            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint2*>(x), static_cast<uint8_t*>(codes), lmin, step);
+    else
+        logfmt_encode_kernel<uint16_t><<<warp_grid(n_tiles), 256, 0, s>>>(
+            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint2*>(x), static_cast<uint16_t*>(codes), lmin, step);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_logfmt_decode(int32_t n_bits, int64_t rows, int64_t cols, const void* codes,
+                                        const float* lmin, const float* step, uint16_t* y,
+                                        moe_stream_t stream) {
+    if (n_bits < 3 || n_bits > 12 || rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!codes || !lmin || !step || !y || !aligned16(codes) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    const int64_t tpr = cols / 128, n_tiles = rows * tpr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_bits <= 8)
+        logfmt_decode_kernel<uint8_t><<<warp_grid(n_tiles), 256, 0, s>>>(
+            n_tiles, tpr, cols, n_bits, static_cast<const uint8_t*>(codes), lmin, step, reinterpret_cast<uint2*>(y));
+    else
+        logfmt_decode_kernel<uint16_t><<<warp_grid(n_tiles), 256, 0, s>>>(
+            n_tiles, tpr, cols, n_bits, static_cast<const uint16_t*>(codes), lmin, step, reinterpret_cast<uint2*>(y));
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}

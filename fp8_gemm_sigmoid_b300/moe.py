@@ -63,6 +63,8 @@ _SIGS = {
     "moe_pipeline_submit": [_vp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp, _vp],
     "moe_pipeline_wait": [_vp],
     "moe_pipeline_destroy": [_vp],
+    "moe_logfmt_encode": [_i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
+    "moe_logfmt_decode": [_i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
 }
 
 
@@ -199,6 +201,20 @@ def moe_permute_noalloc(cfg, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as
     _check("moe_permute_noalloc", f(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx), _ptr(xq), _ptr(xs),
                                     _ptr(offs), _ptr(perm_tok), _ptr(row_of), _ptr(aq), _ptr(as_),
                                     _stream(stream)))
+
+
+def moe_logfmt_encode(n_bits, x, codes, lmin, step, stream=None):
+    """x [rows, cols] BF16 (bits as uint16); codes uint8 (n_bits <= 8) or uint16 [rows, cols];
+    lmin, step float32 [rows, cols/128]."""
+    rows, cols = x.shape
+    _check("moe_logfmt_encode", _lib_handle().moe_logfmt_encode(
+        int(n_bits), rows, cols, _ptr(x), _ptr(codes), _ptr(lmin), _ptr(step), _stream(stream)))
+
+
+def moe_logfmt_decode(n_bits, codes, lmin, step, y, stream=None):
+    rows, cols = codes.shape
+    _check("moe_logfmt_decode", _lib_handle().moe_logfmt_decode(
+        int(n_bits), rows, cols, _ptr(codes), _ptr(lmin), _ptr(step), _ptr(y), _stream(stream)))
 
 
 def moe_device_error():

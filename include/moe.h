@@ -283,6 +283,27 @@ MOE_API moe_status moe_pipeline_wait(moe_pipeline* pl);
 /* Waits for the pipeline's work, then releases its streams and events (NULL: no-op). */
 MOE_API moe_status moe_pipeline_destroy(moe_pipeline* pl);
 
+/* LogFMT-nBit, the logarithmic code for the combine payload ([P2] §3.2, LogFMT communication
+ * compression), for 1x128 tiles of a BF16 matrix.  Per tile: min and max of the natural logs
+ * of the non-zero magnitudes (min held above max - ln 2^32) and Step = (max - min) /
+ * (2^(n-1) - 2); each value gets the n-bit code S|K, S its sign bit and K the index of the
+ * value of the grid {0} u {exp(min + Step (K - 1)) : K = 1 .. 2^(n-1) - 1} nearest to its
+ * magnitude in linear space (ties to the larger K); a tile of zeros has min = Step = 0, a tile
+ * of one magnitude Step = 0 and K = 1.
+ *  n_bits: 3 .. 12 (the précis evaluates 8 and 10; above 12 the FP32 tile metadata cannot
+ *  place the grid to a fraction of its step).  x [rows, cols] BF16, cols % 128 == 0;
+ *  codes [rows, cols]: uint8 for n_bits <= 8, uint16 otherwise; lmin, step [rows, cols/128]
+ *  FP32 (the tile metadata).
+ *  x and codes 16-byte aligned.  rows == 0 enqueues nothing. */
+MOE_API moe_status moe_logfmt_encode(int32_t n_bits, int64_t rows, int64_t cols, const uint16_t* x,
+                                     void* codes, float* lmin, float* step, moe_stream_t stream);
+
+/* The inverse: y = (S ? -1 : 1) * (K ? exp(min + Step (K - 1)) : 0), rounded to BF16.
+ *  Same shapes and rules as moe_logfmt_encode; y [rows, cols] BF16, 16-byte aligned. */
+MOE_API moe_status moe_logfmt_decode(int32_t n_bits, int64_t rows, int64_t cols, const void* codes,
+                                     const float* lmin, const float* step, uint16_t* y,
+                                     moe_stream_t stream);
+
 /* Device-side error word written by bounded waits inside the kernels (0 = none).  Reading
  * it synchronises the device.  *code receives the word; the call then clears it. */
 MOE_API moe_status moe_device_error(int32_t* code);

@@ -200,3 +200,17 @@ def test_more_host_side_rejections(moe):
     assert L.moe_selftest_wait_timeout(0, None) == INV
     assert L.moe_selftest_wait_timeout(4000000001, None) == INV
     assert L.moe_device_error(None) == INV
+
+
+def test_logfmt_host_side_rejections(moe):
+    L = moe._lib_handle()
+    vp = ctypes.c_void_p
+    INV = moe.MOE_ERR_INVALID_ARG
+    for f in (L.moe_logfmt_encode, L.moe_logfmt_decode):
+        assert f(8, 0, 128, None, None, None, None, None) == moe.MOE_OK  # no rows: nothing to do
+        assert f(2, 4, 128, vp(16), vp(16), vp(16), vp(16), None) == INV  # n_bits below 3
+        assert f(13, 4, 128, vp(16), vp(16), vp(16), vp(16), None) == INV  # above 12
+        assert f(8, 4, 100, vp(16), vp(16), vp(16), vp(16), None) == INV   # cols not a multiple of 128
+        assert f(8, -1, 128, vp(16), vp(16), vp(16), vp(16), None) == INV
+        assert f(8, 4, 128, vp(16), vp(16), None, vp(16), None) == INV
+        assert f(8, 4, 128, vp(24), vp(16), vp(16), vp(16), None) == INV  # misaligned
