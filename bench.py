@@ -48,6 +48,10 @@ def parse():
     p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--config", default="v3_prefill", choices=sorted(sy.CONFIGS))
+    p.add_argument("--mode", default=None, choices=["fp8", "mxfp8"],
+                   help="quantisation mode of the timed layer (default: the workload's, FP32 scales)")
+    p.add_argument("--no-mxfp8", action="store_true",
+                   help="skip the secondary measurement of the power-of-two (MXFP8) mode")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-sample", type=int, default=512,
                    help="tokens of the seeded sample on which the oracle's expert FFNs are timed")
@@ -157,13 +161,19 @@ class Clocks:
 class Layer:
     """Device-resident inputs, FP8 weights, outputs, staged intermediates and workspace."""
 
-    def __init__(self, cfg, dev, keep_bf16=True):
+    def __init__(self, cfg, dev, keep_bf16=True, inp=None, extra_modes=(), q=None):
+        """inp: inputs to share with another Layer; q: its FP8 weights, already quantised;
+        extra_modes: other quantisation modes whose FP8 weights are made before the BF16
+        weights are dropped (self.extra_q[mode])."""
         self.cfg = cfg
         T, H, I, E, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["n_experts"], cfg["top_k"]
         S = int(cfg["has_shared"])
-        self.inp = sy.make_inputs(cfg, dev)
-        self.q = moe.quantize_weights(self.inp["W13"], self.inp["W2"])
-        if not keep_bf16:  # the BF16 expert weights only feed the CPU oracle
+        self.mx = cfg["mode"] == "mxfp8"
+        self.inp = inp if inp is not None else sy.make_inputs(cfg, dev)
+        self.q = q if q is not None else moe.quantize_weights(self.inp["W13"], self.inp["W2"], pow2=self.mx)
+        self.extra_q = {m: moe.quantize_weights(self.inp["W13"], self.inp["W2"], pow2=(m == "mxfp8"))
+                        for m in extra_modes}
+        if not keep_bf16 and "W13" in self.inp:  # the BF16 expert weights only feed the CPU oracle
             del self.inp["W13"], self.inp["W2"]
             torch.cuda.empty_cache()
         self.x = self.inp["x"].view(torch.uint16)
@@ -209,16 +219,27 @@ class Layer:
         ev[0].record()
         moe.moe_gate(c, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"])
         ev[1].record()
-        moe.moe_quant_1x128(self.x, self.xq, self.xs)
+        if self.mx:
+            moe.moe_quant_1x128_pow2(self.x, self.xq, self.xs)
+        else:
+            moe.moe_quant_1x128(self.x, self.xq, self.xs)
         ev[2].record()
         moe.moe_permute(c, T, o["topk_idx"], o["counts"], self.xq, self.xs, self.offs, self.perm_tok,
                         self.row_of, self.aq, self.as_, self.ws)
         ev[3].record()
-        moe.moe_grouped_gemm_fp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
-                                 self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs, self.ws)
+        if self.mx:
+            moe.moe_grouped_gemm_mxfp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
+                                       self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs)
+        else:
+            moe.moe_grouped_gemm_fp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
+                                     self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs, self.ws)
         ev[4].record()
-        moe.moe_grouped_gemm_fp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
-                                 self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None, self.ws)
+        if self.mx:
+            moe.moe_grouped_gemm_mxfp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
+                                       self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None)
+        else:
+            moe.moe_grouped_gemm_fp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
+                                     self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None, self.ws)
         ev[5].record()
         ysh = self.yexp[T * c["top_k"]:] if c["has_shared"] else None
         moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], ysh, self.y)
@@ -314,6 +335,8 @@ class OracleLayer:
         import numpy as np
         import oracle
         self.np, self.oracle, self.cfg = np, oracle, cfg
+        self.pow2 = cfg["mode"] == "mxfp8"
+        self.ocfg = dict(cfg, mode="fp8_pow2") if self.pow2 else cfg  # the oracle's name of the mode
         self.x = layer.inp["x"].view(torch.uint16).cpu().numpy()
         self.Wg = layer.inp["Wg"].view(torch.uint16).cpu().numpy()
         self.bias = layer.inp["bias"].cpu().numpy()
@@ -327,7 +350,7 @@ class OracleLayer:
             idx = torch.tensor(miss, device=self.W13.device)
             w13 = self.W13.index_select(0, idx).view(torch.uint16).cpu().numpy()
             w2 = self.W2.index_select(0, idx).view(torch.uint16).cpu().numpy()
-            q = self.oracle.quantize_weights(w13, w2)
+            q = self.oracle.quantize_weights(w13, w2, pow2=self.pow2)
             for j, e in enumerate(miss):
                 self.cache[e] = tuple(a[j:j + 1] for a in q)
         return tuple(np.concatenate([self.cache[int(e)][i] for e in ids]) for i in range(4))
@@ -353,7 +376,7 @@ class OracleLayer:
         t1 = time.perf_counter()
         self.prepare(g, sample)
         t2 = time.perf_counter()
-        self.oracle.experts_and_combine(c, self.x[gate_tokens], g, sample, None, None, qweights=self.qweights)
+        self.oracle.experts_and_combine(self.ocfg, self.x[gate_tokens], g, sample, None, None, qweights=self.qweights)
         t3 = time.perf_counter()
         return t1 - t0, t3 - t2
 
@@ -505,6 +528,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     over = {k: v for k, v in (("T", args.T), ("n_experts", args.experts), ("n_group", args.groups),
                               ("topk_group", args.topk_group)) if v is not None}
+    if args.mode is not None:
+        over["mode"] = args.mode
     cfg = sy.config(args.config, **over)
     if args.only:
         return run_only(args, cfg)
@@ -518,7 +543,8 @@ def main():
     peaks = load_peaks()
     T = cfg["T"]
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    layer = Layer(cfg, dev, keep_bf16=want_cpu)
+    want_mx = cfg["mode"] == "fp8" and not args.no_mxfp8
+    layer = Layer(cfg, dev, keep_bf16=want_cpu, extra_modes=("mxfp8",) if want_mx else ())
     stream = torch.cuda.current_stream()
 
     # warm-up (W whole-layer steps through moe_forward and through the staged calls)
@@ -625,6 +651,37 @@ def main():
             t_ms = a.elapsed_time(b) / args.steps
             logfmt[name] = {"ms": t_ms, "GB/s": nbytes / t_ms / 1e6, "frac_hbm": nbytes / t_ms / 1e6 / peaks["hbm"]}
         del codes, lmin, lstep, back
+    # the same layer in power-of-two (MXFP8) mode: tensor cores apply the scales themselves
+    mxfp8 = None
+    if want_mx:
+        cfg_mx = dict(cfg, mode="mxfp8")
+        lmx = Layer(cfg_mx, dev, keep_bf16=False, inp=layer.inp, q=layer.extra_q.pop("mxfp8"))
+        for _ in range(3):
+            lmx.forward(world)
+        barrier_sync(dist_on)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            lmx.forward(world)
+        b.record(stream)
+        barrier_sync(dist_on)
+        mx_value, mx_ms = replica_throughput(T, args.steps, a.elapsed_time(b), dist_on)
+        evs_mx = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+        for evs in evs_mx:
+            lmx.staged(evs, world)
+        barrier_sync(dist_on)
+        assert moe.moe_device_error() == 0
+        g1 = sum(evs[3].elapsed_time(evs[4]) for evs in evs_mx) / args.steps
+        g2 = sum(evs[4].elapsed_time(evs[5]) for evs in evs_mx) / args.steps
+        w_mx = stage_work(cfg)
+        mxfp8 = {"value": mx_value, "unit": "tokens/s", "ms_per_step": mx_ms / args.steps,
+                 "gemm1_swiglu": {"ms": g1, "TFLOP/s": w_mx["gemm1_swiglu"][1] / g1 / 1e9,
+                                  "frac_fp8_peak": w_mx["gemm1_swiglu"][1] / g1 / 1e9 / (peaks["bf16"] * FP8_PER_BF16)},
+                 "gemm2_down": {"ms": g2, "TFLOP/s": w_mx["gemm2_down"][1] / g2 / 1e9,
+                                "frac_fp8_peak": w_mx["gemm2_down"][1] / g2 / 1e9 / (peaks["bf16"] * FP8_PER_BF16)},
+                 "dtype": "fp8-e4m3, power-of-two 1x128 / 128x128 scales applied by the tensor cores"}
+        del lmx
+        torch.cuda.empty_cache()
     clocks.stop()
     clk = clocks.stats(*r1)
     stage_clk = clocks.stats(*r2)
@@ -678,7 +735,8 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8-e4m3 (FP32 accumulation), bf16 activations",
+        "dtype": ("fp8-e4m3 (FP32 accumulation), bf16 activations" if cfg["mode"] == "fp8" else
+                  "fp8-e4m3, power-of-two scales applied by the tensor cores, bf16 activations"),
         "data": "synthetic",
         "config": config_dict(cfg, world),
         "grouped_gemm": {"ms": gemm_ms, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak,
@@ -686,6 +744,7 @@ def main():
         "stages": stages,
         "staged_steps": n_staged,
         "logfmt": logfmt,
+        "mxfp8": mxfp8,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,

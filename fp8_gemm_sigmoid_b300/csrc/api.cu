@@ -41,7 +41,7 @@ bool config_ok(const moe_config* c) {
     if (c->top_k > c->topk_group * (c->n_experts / c->n_group)) return false;
     if (c->n_experts > 1024 || c->top_k > 32) return false;
     if (c->has_shared != 0 && c->has_shared != 1) return false;
-    if (c->mode != MOE_FP32 && c->mode != MOE_FP8_BLOCK) return false;
+    if (c->mode != MOE_FP32 && c->mode != MOE_FP8_BLOCK && c->mode != MOE_MXFP8) return false;
     if (c->hidden % 128 != 0 || c->inter % 128 != 0) return false;
     return true;
 }
@@ -51,7 +51,7 @@ static size_t align_up(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023
 WsLayout ws_layout(const moe_config& c, int64_t T) {
     WsLayout L{};
     const int64_t H = c.hidden, I = c.inter, E = c.n_experts, K = c.top_k, S = c.has_shared;
-    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const bool fp8 = (c.mode != MOE_FP32);
     const int64_t R = T * K + T * S;
     L.R = R;
     size_t o = 0;
@@ -106,10 +106,11 @@ extern "C" moe_status moe_device_error(int32_t* code) {
     MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
     const int zero = 0;
     MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
-    int32_t tc = 0, gate = 0;
+    int32_t tc = 0, mx = 0, gate = 0;
     MOE_TRY(tc_read_and_clear_error(&tc));
+    MOE_TRY(mx_read_and_clear_error(&mx));
     MOE_TRY(gate_read_and_clear_error(&gate));
-    *code = v ? v : (tc ? tc : gate);
+    *code = v ? v : (tc ? tc : (mx ? mx : gate));
     return MOE_OK;
 }
 
@@ -157,7 +158,8 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
                                   void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (!config_ok(cfg) || T < 0 || !w || !counts || !ws || !bias) return MOE_ERR_INVALID_ARG;
     const moe_config& c = *cfg;
-    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const bool fp8 = (c.mode != MOE_FP32);
+    const bool mx = (c.mode == MOE_MXFP8);
     if (!w->Wg || !w->W13 || !w->W2 || (fp8 && (!w->W13_s || !w->W2_s))) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !y || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(ws) || (T > 0 && (!aligned16(x) || !aligned16(y)))) return MOE_ERR_INVALID_ARG;
@@ -183,15 +185,24 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
         uint8_t* hq = reinterpret_cast<uint8_t*>(base + L.hq);
         float* hs = reinterpret_cast<float*>(base + L.hs);
         void* yexp = base + L.yexp;
-        MOE_TRY(moe_quant_1x128(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
+        if (mx) MOE_TRY(moe_quant_1x128_pow2(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
+        else MOE_TRY(moe_quant_1x128(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
         MOE_TRY(moe_permute(cfg, T, topk_idx, counts, xq, xs, offs, perm_tok, row_of, aq, as, ws,
                             ws_bytes, stream));
-        MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, static_cast<int32_t>(2 * I), static_cast<int32_t>(H),
-                                     aq, as, static_cast<const uint8_t*>(w->W13), w->W13_s,
-                                     MOE_EPI_SWIGLU_QUANT, hq, hs, gscratch, gbytes, stream));
-        MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, static_cast<int32_t>(H), static_cast<int32_t>(I),
-                                     hq, hs, static_cast<const uint8_t*>(w->W2), w->W2_s,
-                                     MOE_EPI_STORE, yexp, nullptr, gscratch, gbytes, stream));
+        const int32_t N1 = static_cast<int32_t>(2 * I), N2 = static_cast<int32_t>(H);
+        const uint8_t* W13 = static_cast<const uint8_t*>(w->W13);
+        const uint8_t* W2 = static_cast<const uint8_t*>(w->W2);
+        if (mx) {
+            MOE_TRY(moe_grouped_gemm_mxfp8(G, offs, L.R, N1, N2, aq, as, W13, w->W13_s, MOE_EPI_SWIGLU_QUANT,
+                                           hq, hs, stream));
+            MOE_TRY(moe_grouped_gemm_mxfp8(G, offs, L.R, N2, static_cast<int32_t>(I), hq, hs, W2, w->W2_s,
+                                           MOE_EPI_STORE, yexp, nullptr, stream));
+        } else {
+            MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, N1, N2, aq, as, W13, w->W13_s, MOE_EPI_SWIGLU_QUANT,
+                                         hq, hs, gscratch, gbytes, stream));
+            MOE_TRY(moe_grouped_gemm_fp8(G, offs, L.R, N2, static_cast<int32_t>(I), hq, hs, W2, w->W2_s,
+                                         MOE_EPI_STORE, yexp, nullptr, gscratch, gbytes, stream));
+        }
         const void* yshared = c.has_shared ? static_cast<const char*>(yexp) + T * c.top_k * H * 2 : nullptr;
         MOE_TRY(moe_combine(cfg, T, yexp, row_of, topk_w, yshared, y, stream));
     } else {

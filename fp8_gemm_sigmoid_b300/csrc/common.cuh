@@ -83,6 +83,30 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
     return __uint_as_float(__float_as_uint(mag) | s);
 }
 
+// Power-of-two block scales (the 8-bit exponent scales of microscaling): for a tile with
+// amax > 0 the exponent is the smallest e with 448 * 2^e >= amax.  With amax = m * 2^E,
+// m in [1, 2), and 448 = 1.75 * 2^8 that is E - 8 when m <= 1.75 and E - 7 otherwise; a
+// subnormal amax (below 2^-126) gives the floor -127.  Clamped to [-127, 127].
+__device__ __forceinline__ int pow2_exponent(float amax) {
+    if (amax < 1.17549435e-38f) return -127;
+    const uint32_t u = __float_as_uint(amax);
+    const int E = static_cast<int>((u >> 23) & 0xffu) - 127;
+    const int e = E - 8 + ((u & 0x7fffffu) > 0x600000u ? 1 : 0);  // significand above 1.75
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^e as an FP32 value for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2_int(int e) {
+    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// v * 2^-e for e in [-127, 127]: two exact power-of-two factors, so the product is exact
+// whenever it is a normal FP32 value.
+__device__ __forceinline__ float scale_pow2(float v, int e) {
+    const int h = -e / 2;
+    return (v * exp2_int(h)) * exp2_int(-e - h);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

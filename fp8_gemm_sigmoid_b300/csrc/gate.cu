@@ -470,7 +470,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 
 bool gate_tc_supported(const moe_config& c) {
     const int E = c.n_experts, G = c.n_group;
-    return c.mode == MOE_FP8_BLOCK && E % 32 == 0 && E <= kGtMaxE && G <= kGtMaxG &&
+    return c.mode != MOE_FP32 && E % 32 == 0 && E <= kGtMaxE && G <= kGtMaxG &&
            (E / G) % 32 == 0 && c.top_k <= kGtMaxK && c.hidden % kGtK == 0;
 }
 

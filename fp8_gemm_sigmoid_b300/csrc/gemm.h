@@ -25,6 +25,10 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
                                       int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
                                       const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
                                       cudaStream_t s);
+moe_status launch_grouped_gemm_mxf8(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N, int32_t Kd,
+                                    const uint8_t* A, const float* As, const uint8_t* W, const float* Ws,
+                                    int32_t epilogue, void* out, float* out_s, cudaStream_t s);
+moe_status mx_read_and_clear_error(int32_t* code);
 size_t tc_scratch_bytes(int32_t n_groups);
 constexpr int32_t kMaxGemmGroups = 1040;  // groups of one grouped-GEMM call (tile schedule in shared memory)
 moe_status tc_read_and_clear_error(int32_t* code);

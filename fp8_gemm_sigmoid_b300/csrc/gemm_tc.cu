@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "internal.h"
+#include "gemm_sched.cuh"
 #include "sm100.cuh"
 
 namespace moe {
@@ -42,8 +43,9 @@ __device__ int g_tc_error = 0;
 namespace {
 
 using namespace sm100;
+using namespace sched;
 
-constexpr int kBM = 128, kBN = 256, kBK = 128;
+constexpr int kBK = 128;
 constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
@@ -72,56 +74,14 @@ constexpr int kSmemMax = kSmemFixed + 4 * (kMaxGroups + 1);
 enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103,
              kErrTimeoutScales = 0x104 };
 
-struct TcParams {
-    int n_groups;
-    const int32_t* offs;        // [n_groups + 1]
-    int N;                      // rows of W per group
+struct TcParams : sched::Groups {  // n_groups, offs, N, n_tiles_n, swiglu
     int nkb;                    // K / 128
     int rows;                   // row capacity of A, As and out
-    int n_tiles_n;              // 256-column tiles per group
-    int swiglu;                 // 1: gate/up pairing + FP8 re-quantisation; 0: BF16 store
     const float* As;            // [nkb, rows] (K-block-major)
     const float* Ws;            // [n_groups, N/128, nkb]
     void* out;                  // SwiGLU: [rows, N/2] E4M3; store: [rows, N] BF16
     float* out_s;               // SwiGLU: [N/256, rows] (K-block-major, as the next GEMM reads it)
 };
-
-constexpr int kNFastMTiles = 32;  // m-tiles (4096 rows) above which a group runs n-fastest
-
-struct TileCoord {
-    int g, m_local, n_tile;
-    int row0, row_end;
-};
-
-// Tile t of the schedule.  In a group of up to kNFastMTiles m-tiles the m-tiles run fastest:
-// the concurrent tiles share each weight tile in L2.  A larger group (the shared expert's T
-// rows) runs its n-tiles fastest instead, so that its A rows, which would not stay in L2
-// between n-tiles, are read once while its weight tiles stay in L2.
-__device__ __forceinline__ TileCoord decode_tile(const TcParams& p, const int32_t* tile_start, int t) {
-    TileCoord c;
-    c.g = find_group(tile_start, p.n_groups, t);
-    const int local = t - tile_start[c.g];
-    c.row0 = p.offs[c.g];
-    c.row_end = p.offs[c.g + 1];
-    const int mt = (c.row_end - c.row0 + kBM - 1) / kBM;
-    if (mt > kNFastMTiles) {  // a large group: its n-tiles run fastest, each A tile is read once
-        c.m_local = local / p.n_tiles_n;
-        c.n_tile = local - c.m_local * p.n_tiles_n;
-    } else {
-        c.n_tile = local / mt;
-        c.m_local = local - c.n_tile * mt;
-    }
-    c.row0 += c.m_local * kBM;
-    return c;
-}
-
-// Row of W (flattened [n_groups * N, K]) and scale block of the two 128-row halves of the
-// tile's B operand.  SwiGLU pairs gate block n_tile with the up block I/128 + n_tile, so
-// column j of the first half and column 128 + j of the second half belong to the same h.
-__device__ __forceinline__ int b_block(const TcParams& p, const TileCoord& c, int half) {
-    if (p.swiglu) return half == 0 ? c.n_tile : (p.N / 2) / 128 + c.n_tile;
-    return 2 * c.n_tile + half;
-}
 
 // acc[base + i] += (r[2i], r[2i+1]) * (s, s) for i < 8: one packed FP32x2 FMA per column pair,
 // each lane rounded as a separate fmaf.
@@ -140,60 +100,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 2D TMA store of a [32 rows x 128 B] box from shared memory (128-byte swizzle) at (x, y).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Tiles of group g: ceil(rows_g / 128) m-tiles times the n-tiles of one group.
-__device__ __forceinline__ int group_tiles(const TcParams& p, int g) {
-    return ((p.offs[g + 1] - p.offs[g] + kBM - 1) / kBM) * p.n_tiles_n;
-}
-
-// tile_start[g] = tiles of the groups before g (g = 0..n_groups), computed by the whole CTA
-// from the device-side row offsets: each thread sums a run of consecutive groups, a block
-// scan of the run totals gives each run's start, and the thread writes its run's prefixes.
-__device__ void tile_prefix(const TcParams& p, int32_t* warp_sums, int32_t* tile_start) {
-    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-    const int per = (p.n_groups + kThreads - 1) / kThreads;
-    const int g0 = min(tid * per, p.n_groups), g1 = min(g0 + per, p.n_groups);
-    int sum = 0;
-    for (int g = g0; g < g1; ++g) sum += group_tiles(p, g);
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < kThreads / 32 ? warp_sums[lane] : 0;
-        const int own = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += v;
-        }
-        if (lane < kThreads / 32) warp_sums[lane] = w - own;  // exclusive warp offsets
-    }
-    __syncthreads();
-    int run = warp_sums[warp] + incl - sum;
-    for (int g = g0; g < g1; ++g) {
-        tile_start[g] = run;
-        run += group_tiles(p, g);
-    }
-    if (g0 < g1 && g1 == p.n_groups) tile_start[p.n_groups] = run;
-    __syncthreads();
-}
 
 // silu(g) = g * sigmoid(g) with the fast exponential and division intrinsics: h is quantised
 // to E4M3 (3 mantissa bits) right after, so their few-ulp FP32 error only matters on a code
@@ -254,7 +160,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!p.swiglu) tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
-    tile_prefix(p, warp_sums, tile_start);  // contains the CTA barriers that publish the set-up
+    tile_prefix<kThreads>(p, warp_sums, tile_start);  // contains the CTA barriers that publish the set-up
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = tile_start[p.n_groups];

@@ -26,6 +26,7 @@ namespace {
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 constexpr float kLog2eLo = 1.925963033500011e-08f;  // log2(e) - kLog2e
+constexpr int kTilesInFlight = 4;  // tiles per warp and step, loaded together
 
 __device__ __forceinline__ float warp_min(float v) {
 #pragma unroll
@@ -61,10 +62,21 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
     const int kmax = (1 << (n_bits - 1)) - 1;
     const uint32_t sign_bit = 1u << (n_bits - 1);
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tiles;
-         t += nwarps) {
+    // kTilesInFlight tiles per warp and step: their loads are issued together
+    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesInFlight;
+         t0 < n_tiles; t0 += nwarps * kTilesInFlight) {
+      uint2 raws[kTilesInFlight];
+#pragma unroll
+      for (int j = 0; j < kTilesInFlight; ++j) {
+        const int64_t t = t0 + j < n_tiles ? t0 + j : t0;
+        raws[j] = x[((t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4) / 4];
+      }
+#pragma unroll
+      for (int j = 0; j < kTilesInFlight; ++j) {
+        const int64_t t = t0 + j;
+        if (t >= n_tiles) break;
         const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
-        const uint2 raw = x[base / 4];
+        const uint2 raw = raws[j];
         float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
         float amax = 0.f, amin = INFINITY;
@@ -123,6 +135,7 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             lmin_out[t] = l2min * kLn2;
             step_out[t] = step2 * kLn2;
         }
+      }
     }
 }
 
@@ -134,21 +147,36 @@ logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
     const int lane = threadIdx.x & 31;
     const uint32_t kmask = (1u << (n_bits - 1)) - 1u;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tiles;
-         t += nwarps) {
+    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesInFlight;
+         t0 < n_tiles; t0 += nwarps * kTilesInFlight) {
+      uint2 raws[kTilesInFlight];
+      float lms[kTilesInFlight], sts[kTilesInFlight];
+#pragma unroll
+      for (int j = 0; j < kTilesInFlight; ++j) {  // every load of the step in flight together
+        const int64_t t = t0 + j < n_tiles ? t0 + j : t0;
+        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
+        if (sizeof(CodeT) == 1) raws[j] = make_uint2(*reinterpret_cast<const uint32_t*>(codes + base), 0u);
+        else raws[j] = *reinterpret_cast<const uint2*>(codes + base);
+        lms[j] = lmin[t];
+        sts[j] = step[t];
+      }
+#pragma unroll
+      for (int j = 0; j < kTilesInFlight; ++j) {
+        const int64_t t = t0 + j;
+        if (t >= n_tiles) break;
         const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
         uint32_t c[4];
         if (sizeof(CodeT) == 1) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + base);
+            const uint32_t w = raws[j].x;
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[i] = (w >> (8 * i)) & 0xffu;
         } else {
-            const uint2 w = *reinterpret_cast<const uint2*>(codes + base);
+            const uint2 w = raws[j];
             c[0] = w.x & 0xffffu; c[1] = w.x >> 16; c[2] = w.y & 0xffffu; c[3] = w.y >> 16;
         }
         // g1 = e^min once per tile; Step2 = Step * log2(e) as an exact pair (hi + lo)
-        const float st = step[t];
-        const float g1 = expf(lmin[t]);
+        const float st = sts[j];
+        const float g1 = expf(lms[j]);
         const float s_hi = st * kLog2e;
         const float s_lo = fmaf(st, kLog2e, -s_hi) + st * kLog2eLo;
         uint16_t o[4];
@@ -167,11 +195,12 @@ logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             o[i] = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
         }
         y[base / 4] = make_uint2(o[0] | (static_cast<uint32_t>(o[1]) << 16), o[2] | (static_cast<uint32_t>(o[3]) << 16));
+      }
     }
 }
 
 unsigned warp_grid(int64_t n_tiles) {
-    const int64_t blocks = ceil_div(n_tiles, 8);
+    const int64_t blocks = ceil_div(n_tiles, 8 * kTilesInFlight);
     return static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
 }
 

@@ -302,7 +302,7 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
                           const float* xs, int32_t* offs, int32_t* perm_tok, int32_t* row_of, void* aq,
                           float* as, int32_t* chunk_cnt, int32_t* chunk_base, cudaStream_t s) {
     const int E = c.n_experts, K = c.top_k, S = c.has_shared;
-    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const bool fp8 = (c.mode != MOE_FP32);
     const int64_t n_chunks = ceil_div(T, kChunk);
     chunk_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * E, s>>>(T, K, E, topk_idx,
                                                                                        chunk_cnt);
@@ -351,7 +351,7 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     if (!config_ok(cfg) || T < 0) return MOE_ERR_INVALID_ARG;
     const moe_config& c = *cfg;
     const int E = c.n_experts, K = c.top_k, S = c.has_shared;
-    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const bool fp8 = (c.mode != MOE_FP32);
     if (!offs || !ws) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe::ws_layout(c, T).total) return MOE_ERR_WORKSPACE;
     if (T > 0 && (!topk_idx || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
@@ -412,7 +412,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, int64_t T,
     if (!config_ok(cfg) || T < 0) return MOE_ERR_INVALID_ARG;
     const moe_config& c = *cfg;
     const int E = c.n_experts, K = c.top_k, S = c.has_shared;
-    const bool fp8 = (c.mode == MOE_FP8_BLOCK);
+    const bool fp8 = (c.mode != MOE_FP32);
     if (!offs) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;

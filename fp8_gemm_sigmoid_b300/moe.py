@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
-MOE_FP32, MOE_FP8_BLOCK = 0, 1
+MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8 = 0, 1, 2
 MOE_EPI_SWIGLU_QUANT, MOE_EPI_STORE = 0, 1
 
 
@@ -48,6 +48,9 @@ _SIGS = {
     "moe_gate": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_quant_1x128": [_i64, _i64, _vp, _vp, _vp, _vp],
     "moe_quant_128x128": [_i64, _i64, _i64, _vp, _vp, _vp, _vp],
+    "moe_quant_1x128_pow2": [_i64, _i64, _vp, _vp, _vp, _vp],
+    "moe_quant_128x128_pow2": [_i64, _i64, _i64, _vp, _vp, _vp, _vp],
+    "moe_grouped_gemm_mxfp8": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp],
     "moe_permute": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_fp8": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                              _vp, _sz, _vp],
@@ -112,8 +115,8 @@ def _stream(stream=None):
 
 def make_config(cfg):
     """moe_config from a workload dict (hidden, inter, n_experts, n_group, topk_group,
-    top_k, routed_scaling_factor, has_shared, mode 'fp32' | 'fp8')."""
-    mode = {"fp32": MOE_FP32, "fp8": MOE_FP8_BLOCK}[cfg["mode"]]
+    top_k, routed_scaling_factor, has_shared, mode 'fp32' | 'fp8' | 'mxfp8')."""
+    mode = {"fp32": MOE_FP32, "fp8": MOE_FP8_BLOCK, "mxfp8": MOE_MXFP8}[cfg["mode"]]
     return moe_config(cfg["hidden"], cfg["inter"], cfg["n_experts"], cfg["n_group"],
                       cfg["topk_group"], cfg["top_k"], float(cfg["routed_scaling_factor"]),
                       int(cfg["has_shared"]), mode)
@@ -144,9 +147,22 @@ def moe_quant_1x128(x, q, s, stream=None):
     _check("moe_quant_1x128", _lib_handle().moe_quant_1x128(rows, cols, _ptr(x), _ptr(q), _ptr(s), _stream(stream)))
 
 
-def moe_quant_128x128(w, q, s, stream=None):
+def moe_quant_128x128(w, q, s, stream=None, pow2=False):
     n, rows, cols = w.shape if w.dim() == 3 else (1, *w.shape)
-    _check("moe_quant_128x128", _lib_handle().moe_quant_128x128(n, rows, cols, _ptr(w), _ptr(q), _ptr(s), _stream(stream)))
+    name = "moe_quant_128x128_pow2" if pow2 else "moe_quant_128x128"
+    _check(name, getattr(_lib_handle(), name)(n, rows, cols, _ptr(w), _ptr(q), _ptr(s), _stream(stream)))
+
+
+def moe_quant_1x128_pow2(x, q, s, stream=None):
+    rows, cols = x.shape
+    _check("moe_quant_1x128_pow2", _lib_handle().moe_quant_1x128_pow2(rows, cols, _ptr(x), _ptr(q), _ptr(s),
+                                                                      _stream(stream)))
+
+
+def moe_grouped_gemm_mxfp8(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue, out, out_s, stream=None):
+    _check("moe_grouped_gemm_mxfp8", _lib_handle().moe_grouped_gemm_mxfp8(
+        int(n_groups), _ptr(offs), int(rows), int(N), int(Kdim), _ptr(A), _ptr(As), _ptr(W), _ptr(Ws),
+        int(epilogue), _ptr(out), _ptr(out_s), _stream(stream)))
 
 
 def moe_permute(cfg, T, topk_idx, counts, xq, xs, offs, perm_tok, row_of, aq, as_, ws, stream=None):
@@ -239,14 +255,15 @@ def workspace(cfg, T, device="cuda"):
     return torch.empty((moe_workspace_size(cfg, T),), dtype=torch.uint8, device=device)
 
 
-def quantize_weights(W13, W2, stream=None):
-    """FP8 copies of the stacked BF16 expert weights via moe_quant_128x128."""
+def quantize_weights(W13, W2, stream=None, pow2=False):
+    """FP8 copies of the stacked BF16 expert weights via moe_quant_128x128 (moe_quant_128x128_pow2
+    with pow2: the power-of-two scales of the MXFP8 mode)."""
     out = {}
     for name, W in (("W13", W13), ("W2", W2)):
         n, R, C = W.shape
         q = torch.empty((n, R, C), dtype=torch.uint8, device=W.device)
         s = torch.empty((n, R // 128, C // 128), dtype=torch.float32, device=W.device)
-        moe_quant_128x128(W.view(torch.uint16) if W.dtype == torch.bfloat16 else W, q, s, stream)
+        moe_quant_128x128(W.view(torch.uint16) if W.dtype == torch.bfloat16 else W, q, s, stream, pow2=pow2)
         out[name], out[name + "_s"] = q, s
     return out
 

@@ -56,8 +56,12 @@ typedef enum moe_status {
 /* Numerics of the layer. */
 typedef enum moe_mode {
     MOE_FP32 = 0,      /* x, gate weight, expert weights and y in FP32, no quantisation */
-    MOE_FP8_BLOCK = 1  /* x, gate weight and y in BF16; expert GEMMs on E4M3 operands with
-                          1x128 activation and 128x128 weight FP32 scales ([P2] §3.2) */
+    MOE_FP8_BLOCK = 1, /* x, gate weight and y in BF16; expert GEMMs on E4M3 operands with
+                          1x128 activation and 128x128 weight FP32 scales amax/448 ([P2] §3.2) */
+    MOE_MXFP8 = 2      /* as MOE_FP8_BLOCK, but every scale is a power of two (the smallest
+                          2^e with 448 * 2^e >= amax) and the tensor cores apply the scales
+                          themselves ([P2] §3.2: scaling factors taken natively, microscaling);
+                          weights from moe_quant_128x128_pow2 */
 } moe_mode;
 
 /* Layer configuration ([P1] §2.2: hidden_size, n_routed_experts, num_experts_per_tok,
@@ -141,6 +145,15 @@ MOE_API moe_status moe_quant_1x128(int64_t rows, int64_t cols, const uint16_t* x
 MOE_API moe_status moe_quant_128x128(int64_t n_mats, int64_t rows, int64_t cols, const uint16_t* w,
                              uint8_t* q, float* s, moe_stream_t stream);
 
+/* a2 in power-of-two mode ([P2] §3.2, scales the tensor cores take natively): the same tiles
+ * and blocks, scale = 2^e with e the smallest integer such that 448 * 2^e >= amax (clamped to
+ * [-127, 127]; amax == 0 gives scale 1 and q = 0), q = E4M3(x * 2^-e), an exact scaling, so no
+ * value saturates.  Same arguments as moe_quant_1x128 / moe_quant_128x128. */
+MOE_API moe_status moe_quant_1x128_pow2(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q,
+                                        float* s, moe_stream_t stream);
+MOE_API moe_status moe_quant_128x128_pow2(int64_t n_mats, int64_t rows, int64_t cols, const uint16_t* w,
+                                          uint8_t* q, float* s, moe_stream_t stream);
+
 /* a3. [P1] §2.3 token permutation by expert, deterministic: rows are expert-major and,
  * within an expert, in ascending token order (the stable argsort of the flat expert ids).
  * With has_shared, group E follows with every token once, in order, in rows
@@ -209,6 +222,17 @@ MOE_API moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, i
                                 const uint8_t* W, const float* Ws, int32_t epilogue,
                                 void* out, float* out_s, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
+
+/* The grouped expert GEMM of MOE_MXFP8 mode ([P2] §3.2: tensor cores that take the
+ * fine-grained scaling factors natively): as moe_grouped_gemm_fp8, but every scale in As and
+ * Ws must be a power of two 2^e, e in [-127, 127] (as moe_quant_*_pow2 write them), and the
+ * tensor cores apply them as 8-bit exponents, accumulating the whole K in FP32 with no
+ * per-block promotion.  SWIGLU_QUANT re-quantises h with power-of-two scales (out_s holds
+ * 2^e).  A scale that is not a power of two is read as its exponent alone.  No workspace. */
+MOE_API moe_status moe_grouped_gemm_mxfp8(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                          int32_t N, int32_t Kdim, const uint8_t* A, const float* As,
+                                          const uint8_t* W, const float* Ws, int32_t epilogue,
+                                          void* out, float* out_s, moe_stream_t stream);
 
 /* The same grouped GEMM with FP32 operands and no scales (FP32 mode):
  *  A [rows, Kdim] FP32; W [n_groups, N, Kdim] FP32; SWIGLU_QUANT writes h [rows, N/2] FP32
