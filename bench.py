@@ -173,7 +173,7 @@ class Layer:
         self.q = q if q is not None else moe.quantize_weights(self.inp["W13"], self.inp["W2"], pow2=self.mx)
         self.extra_q = {m: moe.quantize_weights(self.inp["W13"], self.inp["W2"], pow2=(m == "mxfp8"))
                         for m in extra_modes}
-        if not keep_bf16 and "W13" in self.inp:  # the BF16 expert weights only feed the CPU oracle
+        if not keep_bf16 and inp is None:  # the BF16 expert weights only feed the CPU oracle
             del self.inp["W13"], self.inp["W2"]
             torch.cuda.empty_cache()
         self.x = self.inp["x"].view(torch.uint16)

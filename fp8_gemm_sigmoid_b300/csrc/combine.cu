@@ -140,3 +140,37 @@ extern "C" moe_status moe_bias_update(const moe_config* cfg, int64_t T, const in
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// Row gather for the expert-parallel dispatch: dst[r] = src[idx[r]] (a zero row where
+// idx[r] < 0), row_bytes a multiple of 16; one thread per 16-byte chunk.
+// ---------------------------------------------------------------------------------------
+namespace moe {
+namespace {
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(int64_t n_rows, int64_t chunks, const int32_t* __restrict__ idx,
+                   const uint4* __restrict__ src, uint4* __restrict__ dst) {
+    const int64_t total = n_rows * chunks;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / chunks, c = i - r * chunks;
+        const int32_t s = idx[r];
+        dst[i] = s < 0 ? make_uint4(0u, 0u, 0u, 0u) : src[static_cast<int64_t>(s) * chunks + c];
+    }
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_gather_rows(int64_t n_rows, int64_t row_bytes, const int32_t* idx, const void* src,
+                                      void* dst, moe_stream_t stream) {
+    if (n_rows < 0 || row_bytes <= 0 || row_bytes % 16) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    if (!idx || !src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+    const int64_t chunks = row_bytes / 16;
+    const int64_t blocks = ceil_div(n_rows * chunks, 256);
+    const unsigned grid = static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
+    gather_rows_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        n_rows, chunks, idx, static_cast<const uint4*>(src), static_cast<uint4*>(dst));
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}

@@ -21,13 +21,16 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int n_group
 
 moe_status launch_tile_prefix(int n_groups, int bm, const int32_t* offs, int32_t* tile_start,
                               cudaStream_t s);
+// gather non-null: row r of A is row gather[r] of A [n_tok, Kd] and As is the row-major
+// [n_tok, Kd/128] scale matrix of those rows (index < 0: a zero row).
 moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N,
                                       int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
                                       const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
-                                      cudaStream_t s);
+                                      cudaStream_t s, const int32_t* gather = nullptr, int64_t n_tok = 0);
 moe_status launch_grouped_gemm_mxf8(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N, int32_t Kd,
                                     const uint8_t* A, const float* As, const uint8_t* W, const float* Ws,
-                                    int32_t epilogue, void* out, float* out_s, cudaStream_t s);
+                                    int32_t epilogue, void* out, float* out_s, cudaStream_t s,
+                                    const int32_t* gather = nullptr, int64_t n_tok = 0);
 moe_status mx_read_and_clear_error(int32_t* code);
 size_t tc_scratch_bytes(int32_t n_groups);
 constexpr int32_t kMaxGemmGroups = 1040;  // groups of one grouped-GEMM call (tile schedule in shared memory)

@@ -73,7 +73,9 @@ struct MxParams : sched::Groups {
     int nkb;                    // K / 128
     int rows;                   // row capacity of A, As and out
     int stages;                 // operand ring depth
-    const float* As;            // [nkb, rows] power-of-two scales (K-block-major)
+    const int32_t* gather;      // non-null: row r of A is token gather[r] of X [n_tok, K], its
+    int n_tok;                  //   scales the row-major Xs [n_tok, nkb] (read through As)
+    const float* As;            // [nkb, rows] power-of-two scales (K-block-major), or Xs
     const float* Ws;            // [n_groups, N/128, nkb] power-of-two scales
     void* out;                  // SwiGLU: [rows, N/2] E4M3; store: [rows, N] BF16
     float* out_s;               // SwiGLU: [N/256, rows] power-of-two scales (K-block-major)
@@ -166,8 +168,10 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     if (warp < kEpiWarp0) {
         // register split: 8 x 128 (producer, MMA, idle, scale writers) + 4 x 232 (epilogue)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 128;");
-        if (warp == 0 && lane == 0) {
+        if (warp == 0 && (lane == 0 || p.gather)) {
             // ---------------------------------------------------------------- producer
+            // One lane issues the A box and the two B boxes of a K block; with a gathered A
+            // every lane gathers four of the tile's 128 rows (tile::gather4) by token index.
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -176,25 +180,40 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 const TileCoord c = decode_tile(p, tile_start, t);
                 const int brow0 = c.g * p.N + b_block(p, c, 0) * 128;
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
+                int32_t tok[4] = {0, 0, 0, 0};
+                if (p.gather)
+                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok);
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget);
+                    if (p.gather) w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+                    if (!w) { ok = false; break; }
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kABytes;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
-                    tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
-                    tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
-                    tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    if (p.gather) {
+                        __syncwarp();
+                        tma_gather4(sa + 512 * lane, &tmA, &full[s], kb * kBK, tok[0], tok[1], tok[2], tok[3]);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
+                    }
+                    if (lane == 0) {
+                        tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
+                        tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
+                    }
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 *abort_flag = 1;
                 atomicCAS(&g_mx_error, 0, kErrTimeoutProducer);
             }
-            for (int i = 0; i < S && i < issued; ++i) {  // let every issued copy land
-                if (--s < 0) { s = S - 1; ph ^= 1u; }
-                mbar_wait(&full[s], ph, never, kWaitBudget);
+            if (lane == 0) {
+                for (int i = 0; i < S && i < issued; ++i) {  // let every issued copy land
+                    if (--s < 0) { s = S - 1; ph ^= 1u; }
+                    mbar_wait(&full[s], ph, never, kWaitBudget);
+                }
             }
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------------------- MMA issuer
@@ -249,14 +268,17 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb;
                 const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
                 const int r = c.row0 + q * 32 + lane;
-                const float* as_col = p.As + (r < c.row_end ? r : c.row0);
+                // this row's scale column (K-block-major As) or, gathered, its token's Xs row
+                const float* as_col = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, 0)) * p.nkb
+                                               : p.As + (r < c.row_end ? r : c.row0);
+                const int64_t kstep = p.gather ? 1 : p.rows;
                 for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += 4) {
                     // four K blocks of scales in flight at a time
                     float a4[4], w0[4], w1[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int kb = kb0 + j < p.nkb ? kb0 + j : kb0;
-                        a4[j] = __ldg(as_col + static_cast<int64_t>(kb) * p.rows);
+                        a4[j] = __ldg(as_col + kb * kstep);
                         w0[j] = __ldg(ws0 + kb);
                         w1[j] = __ldg(ws1 + kb);
                     }
@@ -415,12 +437,18 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 
 moe_status launch_grouped_gemm_mxf8(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N, int32_t Kd,
                                     const uint8_t* A, const float* As, const uint8_t* W, const float* Ws,
-                                    int32_t epilogue, void* out, float* out_s, cudaStream_t s) {
+                                    int32_t epilogue, void* out, float* out_s, cudaStream_t s,
+                                    const int32_t* gather, int64_t n_tok) {
     const bool swiglu = (epilogue == MOE_EPI_SWIGLU_QUANT);
     if (N % 128 != 0 || (swiglu && N % 256 != 0)) return MOE_ERR_INVALID_ARG;
-    if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+    if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL || n_tok > 0x7ffffffeLL)
+        return MOE_ERR_INVALID_ARG;
     CUtensorMap tmA, tmB, tmO;
-    if (!make_map_u8(&tmA, A, rows, Kd)) return MOE_ERR_CUDA;
+    if (gather) {  // A = X [n_tok, K], one-row boxes for tile::gather4
+        if (!make_tma_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, n_tok, Kd, 1, 128)) return MOE_ERR_CUDA;
+    } else if (!make_map_u8(&tmA, A, rows, Kd)) {
+        return MOE_ERR_CUDA;
+    }
     if (!make_map_u8(&tmB, W, static_cast<int64_t>(n_groups) * N, Kd)) return MOE_ERR_CUDA;
     if (swiglu) tmO = tmA;  // unused
     else if (!make_tma_map_2d(&tmO, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, N, 32, 64)) return MOE_ERR_CUDA;
@@ -433,6 +461,8 @@ moe_status launch_grouped_gemm_mxf8(int32_t n_groups, const int32_t* offs, int64
     p.nkb = Kd / kBK;
     p.rows = static_cast<int>(rows);
     p.stages = swiglu ? kMaxStages : 3;  // the down GEMM's output staging takes the 4th stage
+    p.gather = gather;
+    p.n_tok = static_cast<int>(n_tok);
     p.As = As;
     p.Ws = Ws;
     p.out = out;

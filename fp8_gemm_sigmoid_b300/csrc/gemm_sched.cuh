@@ -101,6 +101,28 @@ __device__ void tile_prefix(const Groups& p, int32_t* warp_sums, int32_t* tile_s
     __syncthreads();
 }
 
+// TMA gather of four rows (y0..y3, each one box row of 128 bytes at column x) of a 2D tensor
+// whose box is one row high, into 4 consecutive 128-byte rows of shared memory at dst (128-byte
+// swizzle by destination address, so dst at a 512-byte boundary lands them as rows of an A
+// tile); the bytes are reported to `bar`.  A row index outside the tensor reads zeros.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(x),
+        "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
+
+// Token of row r of a gathered A operand (rows [row0, row_end) of the tile's group): gather[r],
+// with rows past the group's end and unclaimed rows (index < 0) mapped to `none`.
+__device__ __forceinline__ int32_t gather_row(const int32_t* gather, int r, int row_end, int32_t none) {
+    if (r >= row_end) return none;
+    const int32_t t = gather[r];
+    return t < 0 ? none : t;
+}
+
 // 2D TMA store of a [32 rows x 128 B] box from shared memory (128-byte swizzle) at (x, y).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -77,7 +77,9 @@ enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpi
 struct TcParams : sched::Groups {  // n_groups, offs, N, n_tiles_n, swiglu
     int nkb;                    // K / 128
     int rows;                   // row capacity of A, As and out
-    const float* As;            // [nkb, rows] (K-block-major)
+    const int32_t* gather;      // non-null: row r of A is token gather[r] of X [n_tok, K], its
+    int n_tok;                  //   scales the row-major Xs [n_tok, nkb] (read through As)
+    const float* As;            // [nkb, rows] (K-block-major), or Xs when gathering
     const float* Ws;            // [n_groups, N/128, nkb]
     void* out;                  // SwiGLU: [rows, N/2] E4M3; store: [rows, N] BF16
     float* out_s;               // SwiGLU: [N/256, rows] (K-block-major, as the next GEMM reads it)
@@ -168,8 +170,10 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     if (warp < kEpiWarp0) {
         // register split: 4 x 48 (TMA, MMA, scale loader, idle) + 8 x 224 (epilogue) <= 12 x 168
         asm volatile("setmaxnreg.dec.sync.aligned.u32 48;");
-        if (warp == 0 && lane == 0) {
+        if (warp == 0 && (lane == 0 || p.gather)) {
             // ---------------------------------------------------------------- producer
+            // One lane issues the A box and the two B boxes of a K block; with a gathered A
+            // every lane gathers four of the tile's 128 rows (tile::gather4) by token index.
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -178,26 +182,41 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const TileCoord c = decode_tile(p, tile_start, t);
                 const int brow0 = c.g * p.N + b_block(p, c, 0) * 128;
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
+                int32_t tok[4] = {0, 0, 0, 0};
+                if (p.gather)
+                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok);
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget);
+                    if (p.gather) w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+                    if (!w) { ok = false; break; }
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kABytes;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
-                    tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
-                    tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
-                    tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    if (p.gather) {
+                        __syncwarp();
+                        tma_gather4(sa + 512 * lane, &tmA, &full[s], kb * kBK, tok[0], tok[1], tok[2], tok[3]);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[s], kb * kBK, c.row0);
+                    }
+                    if (lane == 0) {
+                        tma_load_2d(sb, &tmB, &full[s], kb * kBK, brow0);
+                        tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
+                    }
                     ++issued;
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 *abort_flag = 1;
                 atomicCAS(&g_tc_error, 0, kErrTimeoutProducer);
             }
             // let every issued copy land before the CTA can exit
-            for (int i = 0; i < kStages && i < issued; ++i) {
-                if (--s < 0) { s = kStages - 1; ph ^= 1u; }
-                mbar_wait(&full[s], ph, never, kWaitBudget);
+            if (lane == 0) {
+                for (int i = 0; i < kStages && i < issued; ++i) {
+                    if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+                    mbar_wait(&full[s], ph, never, kWaitBudget);
+                }
             }
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------------------- MMA issuer
@@ -250,17 +269,23 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int b1 = b_block(p, c, 1);
                 const float* ws0 = p.Ws + (static_cast<int64_t>(c.g) * nbk + b_block(p, c, 0)) * p.nkb;
                 const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
+                // each lane's four rows: their scale columns (K-block-major As: stride rows per
+                // K block) or, gathered, their tokens' rows of Xs (stride 1 per K block)
+                const float* src[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = c.row0 + lane + 32 * j;
+                    src[j] = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, 0)) * p.nkb
+                                      : p.As + (r < c.row_end ? r : c.row0);
+                }
+                const int64_t kstep = p.gather ? 1 : p.rows;
                 for (int kb = 0; kb < p.nkb; ++kb, ++kc) {
                     const int i = kc % kScaleSlots;
                     if (!mbar_wait(&sempty[i], ((sph >> i) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
                     sph ^= 1u << i;
                     float* slot = sring + i * kSlotFloats;
-                    const float* col = p.As + static_cast<int64_t>(kb) * p.rows;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = c.row0 + lane + 32 * j;
-                        cp_async4(slot + lane + 32 * j, col + (r < c.row_end ? r : c.row0));
-                    }
+                    for (int j = 0; j < 4; ++j) cp_async4(slot + lane + 32 * j, src[j] + kb * kstep);
                     if (lane == 0) {
                         cp_async4(slot + 128, ws0 + kb);
                         cp_async4(slot + 129, ws1 + kb);
@@ -486,12 +511,17 @@ size_t tc_scratch_bytes(int32_t) { return 0; }
 moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int64_t rows, int32_t N,
                                       int32_t Kd, const uint8_t* A, const float* As, const uint8_t* W,
                                       const float* Ws, int32_t epilogue, void* out, float* out_s, void* ws,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, const int32_t* gather, int64_t n_tok) {
     const bool swiglu = (epilogue == MOE_EPI_SWIGLU_QUANT);
     if (N % 128 != 0 || (swiglu && N % 256 != 0)) return MOE_ERR_INVALID_ARG;
-    if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+    if (rows > 0x7fffffffLL || static_cast<int64_t>(n_groups) * N > 0x7fffffffLL || n_tok > 0x7ffffffeLL)
+        return MOE_ERR_INVALID_ARG;
     CUtensorMap tmA, tmB, tmO;
-    if (!make_map_u8(&tmA, A, rows, Kd)) return MOE_ERR_CUDA;
+    if (gather) {  // A = X [n_tok, K], one-row boxes for tile::gather4
+        if (!make_tma_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, n_tok, Kd, 1, 128)) return MOE_ERR_CUDA;
+    } else if (!make_map_u8(&tmA, A, rows, Kd)) {
+        return MOE_ERR_CUDA;
+    }
     if (!make_map_u8(&tmB, W, static_cast<int64_t>(n_groups) * N, Kd)) return MOE_ERR_CUDA;
     if (swiglu) tmO = tmA;  // unused
     else if (!make_tma_map_2d(&tmO, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, N, 32, 64)) return MOE_ERR_CUDA;
@@ -504,6 +534,8 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     p.rows = static_cast<int>(rows);
     p.n_tiles_n = swiglu ? (N / 2) / 128 : (N + kBN - 1) / kBN;
     p.swiglu = swiglu ? 1 : 0;
+    p.gather = gather;
+    p.n_tok = static_cast<int>(n_tok);
     p.As = As;
     p.Ws = Ws;
     p.out = out;

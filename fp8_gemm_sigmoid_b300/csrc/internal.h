@@ -16,7 +16,7 @@ struct WsLayout {
     size_t offs;       // [E+2] int32
     size_t perm_tok;   // [R] int32
     size_t row_of;     // [T*K] int32
-    size_t aq, as;     // [R,H] codes (FP32 mode: [R,H] f32), [R,H/128]
+    size_t aq, as;     // [R,H] codes (FP32 mode: [R,H] f32), [H/128,R]
     size_t hq, hs;     // [R,I] codes (FP32 mode: h [R,I] f32), [R,I/128]
     size_t yexp;       // [R,H] BF16 (FP32 mode: f32)
     size_t perm_scratch;  // permutation counters

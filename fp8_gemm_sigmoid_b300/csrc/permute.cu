@@ -319,6 +319,7 @@ moe_status launch_permute(const moe_config& c, int64_t T, const int32_t* topk_id
         positions_kernel<<<static_cast<unsigned>(n_chunks), 256, sizeof(int32_t) * kChunk * K, s>>>(
             T, K, E, S, topk_idx, chunk_base, perm_tok, row_of);
     MOE_LAUNCH_CHECK();
+    if (aq == nullptr) return MOE_OK;  // indices only
     const int64_t R = T * K + T * S;
     const int64_t row_bytes = fp8 ? c.hidden : static_cast<int64_t>(c.hidden) * 4;
     const int64_t tok_blocks = ceil_div(T, 8);
@@ -354,10 +355,12 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
     const bool fp8 = (c.mode != MOE_FP32);
     if (!offs || !ws) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe::ws_layout(c, T).total) return MOE_ERR_WORKSPACE;
-    if (T > 0 && (!topk_idx || !xq || !perm_tok || !row_of || !aq)) return MOE_ERR_INVALID_ARG;
     (void)counts;  // the rows are derived from topk_idx itself
-    if (T > 0 && (!aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;
-    if (fp8 && T > 0 && (!xs || !as || !aligned16(xs) || !aligned16(as))) return MOE_ERR_INVALID_ARG;
+    // FP8 modes: aq and as both NULL ask for the indices only (offs, perm_tok, row_of)
+    const bool rows_too = !(fp8 && aq == nullptr && as == nullptr);
+    if (T > 0 && (!topk_idx || !perm_tok || !row_of)) return MOE_ERR_INVALID_ARG;
+    if (rows_too && T > 0 && (!xq || !aq || !aligned16(xq) || !aligned16(aq))) return MOE_ERR_INVALID_ARG;
+    if (rows_too && fp8 && T > 0 && (!xs || !as || !aligned16(xs) || !aligned16(as))) return MOE_ERR_INVALID_ARG;
     if ((T * K + T) >= 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t n_chunks = ceil_div(T, kChunk);
@@ -368,7 +371,8 @@ extern "C" moe_status moe_permute(const moe_config* cfg, int64_t T, const int32_
         MOE_CUDA_CHECK(cudaMemsetAsync(offs, 0, sizeof(int32_t) * (E + 1 + S), s));
         return MOE_OK;
     }
-    return launch_permute(c, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as, chunk_cnt, chunk_base, s);
+    return launch_permute(c, T, topk_idx, xq, xs, offs, perm_tok, row_of, rows_too ? aq : nullptr, as, chunk_cnt,
+                          chunk_base, s);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -51,6 +51,10 @@ _SIGS = {
     "moe_quant_1x128_pow2": [_i64, _i64, _vp, _vp, _vp, _vp],
     "moe_quant_128x128_pow2": [_i64, _i64, _i64, _vp, _vp, _vp, _vp],
     "moe_grouped_gemm_mxfp8": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp],
+    "moe_grouped_gemm_fp8_gather": [_i32, _vp, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                    _vp],
+    "moe_grouped_gemm_mxfp8_gather": [_i32, _vp, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _vp,
+                                      _vp, _vp],
     "moe_permute": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_fp8": [_i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                              _vp, _sz, _vp],
@@ -66,6 +70,7 @@ _SIGS = {
     "moe_pipeline_submit": [_vp, _i64, _vp, ctypes.POINTER(moe_weights), _vp, _i32, _vp, _vp, _vp, _vp],
     "moe_pipeline_wait": [_vp],
     "moe_pipeline_destroy": [_vp],
+    "moe_gather_rows": [_i64, _i64, _vp, _vp, _vp, _vp],
     "moe_logfmt_encode": [_i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
     "moe_logfmt_decode": [_i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
 }
@@ -180,6 +185,16 @@ def moe_grouped_gemm_fp8(n_groups, offs, rows, N, Kdim, A, As, W, Ws, epilogue, 
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_grouped_gemm_fp8_gather(n_groups, offs, rows, N, Kdim, perm_tok, X, Xs, W, Ws, epilogue, out, out_s,
+                                stream=None, mx=False):
+    """Row r of A is X[perm_tok[r]] (X [T, Kdim] codes, Xs [T, Kdim/128] row-major scales);
+    mx: the power-of-two (MXFP8) kernel."""
+    name = "moe_grouped_gemm_mxfp8_gather" if mx else "moe_grouped_gemm_fp8_gather"
+    _check(name, getattr(_lib_handle(), name)(
+        int(n_groups), _ptr(offs), int(rows), int(N), int(Kdim), _ptr(perm_tok), int(X.shape[0]), _ptr(X),
+        _ptr(Xs), _ptr(W), _ptr(Ws), int(epilogue), _ptr(out), _ptr(out_s), _stream(stream)))
+
+
 def moe_grouped_gemm_f32(n_groups, offs, rows, N, Kdim, A, W, epilogue, out, ws, stream=None):
     _check("moe_grouped_gemm_f32", _lib_handle().moe_grouped_gemm_f32(
         int(n_groups), _ptr(offs), int(rows), int(N), int(Kdim), _ptr(A), _ptr(W), int(epilogue),
@@ -217,6 +232,13 @@ def moe_permute_noalloc(cfg, T, topk_idx, xq, xs, offs, perm_tok, row_of, aq, as
     _check("moe_permute_noalloc", f(ctypes.byref(_cfg(cfg)), int(T), _ptr(topk_idx), _ptr(xq), _ptr(xs),
                                     _ptr(offs), _ptr(perm_tok), _ptr(row_of), _ptr(aq), _ptr(as_),
                                     _stream(stream)))
+
+
+def moe_gather_rows(idx, src, dst, stream=None):
+    """dst[r] = src[idx[r]] row by row (zero rows where idx < 0); src, dst 2-D."""
+    row_bytes = src.shape[1] * src.element_size()
+    _check("moe_gather_rows", _lib_handle().moe_gather_rows(int(idx.numel()), int(row_bytes), _ptr(idx),
+                                                            _ptr(src), _ptr(dst), _stream(stream)))
 
 
 def moe_logfmt_encode(n_bits, x, codes, lmin, step, stream=None):

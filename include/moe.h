@@ -169,6 +169,8 @@ MOE_API moe_status moe_quant_128x128_pow2(int64_t n_mats, int64_t rows, int64_t 
  *            aq [R, H] and as [H/128, R] (K-block-major: as[j * R + r] is the scale of
  *            columns 128j..128j+127 of row r, the layout moe_grouped_gemm_fp8 reads);
  *  FP32 mode: xq is x [T, H] FP32 gathered into aq [R, H] FP32; xs and as are ignored.
+ *  FP8 modes: aq and as both NULL ask for the indices only (offs, perm_tok, row_of; xq and xs
+ *  are then not read), for moe_grouped_gemm_fp8_gather.
  *  Outputs: offs [E + 1 + S] int32: offs[e] = rows of the experts before e (e <= E-1),
  *  offs[E] = T*K, offs[E+1] = T*K + T with the shared expert; perm_tok [R] int32 (token of
  *  each row, -1 for an unclaimed row), row_of [T, K] int32 (row of each (t, k), -1 if dropped).
@@ -223,6 +225,19 @@ MOE_API moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, i
                                 void* out, float* out_s, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
 
+/* [P1] §2.3 with the permuted copy fused away: the same grouped GEMM, with row r of A read
+ * straight from the quantised tokens, A[r] = X[perm_tok[r]] and its scales Xs[perm_tok[r], :],
+ * by TMA gathers of four token rows at a time (on B300 the gate/up GEMM then runs at half the
+ * rate of the box-loaded copy, so moe_forward keeps the copy).  perm_tok [rows] as moe_permute writes it
+ * (entries -1, rows no (token, slot) claims, read as zero rows); X [T, Kdim] E4M3 and Xs
+ * [T, Kdim/128] FP32 row-major (moe_quant_1x128's outputs); the other arguments and the
+ * results as for moe_grouped_gemm_fp8, bit for bit (the same bytes reach the same MMAs). */
+MOE_API moe_status moe_grouped_gemm_fp8_gather(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                               int32_t N, int32_t Kdim, const int32_t* perm_tok,
+                                               int64_t T, const uint8_t* X, const float* Xs,
+                                               const uint8_t* W, const float* Ws, int32_t epilogue,
+                                               void* out, float* out_s, moe_stream_t stream);
+
 /* The grouped expert GEMM of MOE_MXFP8 mode ([P2] §3.2: tensor cores that take the
  * fine-grained scaling factors natively): as moe_grouped_gemm_fp8, but every scale in As and
  * Ws must be a power of two 2^e, e in [-127, 127] (as moe_quant_*_pow2 write them), and the
@@ -233,6 +248,14 @@ MOE_API moe_status moe_grouped_gemm_mxfp8(int32_t n_groups, const int32_t* offs,
                                           int32_t N, int32_t Kdim, const uint8_t* A, const float* As,
                                           const uint8_t* W, const float* Ws, int32_t epilogue,
                                           void* out, float* out_s, moe_stream_t stream);
+
+/* moe_grouped_gemm_mxfp8 with the gathered A operand of moe_grouped_gemm_fp8_gather
+ * (X, Xs from moe_quant_1x128_pow2). */
+MOE_API moe_status moe_grouped_gemm_mxfp8_gather(int32_t n_groups, const int32_t* offs, int64_t rows,
+                                                 int32_t N, int32_t Kdim, const int32_t* perm_tok,
+                                                 int64_t T, const uint8_t* X, const float* Xs,
+                                                 const uint8_t* W, const float* Ws, int32_t epilogue,
+                                                 void* out, float* out_s, moe_stream_t stream);
 
 /* The same grouped GEMM with FP32 operands and no scales (FP32 mode):
  *  A [rows, Kdim] FP32; W [n_groups, N, Kdim] FP32; SWIGLU_QUANT writes h [rows, N/2] FP32
@@ -254,6 +277,13 @@ MOE_API moe_status moe_grouped_gemm_f32(int32_t n_groups, const int32_t* offs, i
 MOE_API moe_status moe_combine(const moe_config* cfg, int64_t T, const void* yexp,
                        const int32_t* row_of, const float* topk_w, const void* yshared,
                        void* y, moe_stream_t stream);
+
+/* Row gather for the expert-parallel dispatch ([P1] §2.3: the rows of the tokens routed to
+ * the experts of each destination, in the permutation's order): dst[r] = src[idx[r]] for
+ * r < n_rows, a zero row where idx[r] < 0.  row_bytes a multiple of 16; src, dst 16-byte
+ * aligned; idx [n_rows] int32 with entries < the row count of src. */
+MOE_API moe_status moe_gather_rows(int64_t n_rows, int64_t row_bytes, const int32_t* idx, const void* src,
+                                   void* dst, moe_stream_t stream);
 
 /* a8. Load-driven selection-bias update (the bias "adjusted from real-time load" of
  * [P1] §2.2): bias[i] += 1e-3 * sign(T*K/E - counts[i]), with the sign taken in integers

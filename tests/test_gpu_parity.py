@@ -519,3 +519,53 @@ def test_layer_v3_full_size(moe, sy, orc, v3, name, n_sample):
     r = _check_layer(moe, sy, orc, cfg, n_sample=n_sample, v3=v3)
     print("%s: flagged=%d compared=%d rel_err=%.3g nonempty_experts=%d max_count=%d" % (
         name, r["flagged"], r["compared"], r["err"], int((r["counts"] > 0).sum()), int(r["counts"].max())))
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_gathered_gemm_equals_the_permuted_copy(moe, orc, mx):
+    """[P1] §2.3's permuted copy of the tokens, fused away: the gate/up GEMM reading its rows
+    from the quantised tokens through perm_tok gives the bytes the same GEMM gives on the
+    permutation's copy, including rows no (token, slot) claims (expert ids out of range)."""
+    T, E, K, H, I = 333, 16, 4, 512, 256
+    rng = np.random.default_rng(55 + mx)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[7, 1] = -1
+    idx[200, 3] = E + 3
+    cfg = dict(hidden=H, inter=I, n_experts=E, n_group=4, topk_group=2, top_k=K, routed_scaling_factor=1.0,
+               has_shared=1, mode="mxfp8" if mx else "fp8")
+    g = torch.Generator(device=DEV).manual_seed(3 + mx)
+    x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
+    W13 = (torch.randn(E + 1, 2 * I, H, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn(E + 1, H, I, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    qw = moe.quantize_weights(W13, W2, pow2=mx)
+    xq = torch.empty(T, H, dtype=torch.uint8, device=DEV)
+    xs = torch.empty(T, H // 128, dtype=torch.float32, device=DEV)
+    (moe.moe_quant_1x128_pow2 if mx else moe.moe_quant_1x128)(x.view(torch.uint16), xq, xs)
+    R = T * K + T
+    offs = torch.empty(E + 2, dtype=torch.int32, device=DEV)
+    perm_tok = torch.empty(R, dtype=torch.int32, device=DEV)
+    row_of = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    aq = torch.empty(R, H, dtype=torch.uint8, device=DEV)
+    as_ = torch.empty(H // 128, R, dtype=torch.float32, device=DEV)
+    moe.moe_permute(cfg, T, torch.from_numpy(idx).to(DEV), None, xq, xs, offs, perm_tok, row_of, aq, as_,
+                    moe.workspace(cfg, T))
+    outs = []
+    for gathered in (False, True):
+        hq = torch.full((R, I), 0x55, dtype=torch.uint8, device=DEV)
+        hs = torch.full((I // 128, R), 3.0, dtype=torch.float32, device=DEV)
+        if gathered:
+            moe.moe_grouped_gemm_fp8_gather(E + 1, offs, R, 2 * I, H, perm_tok, xq, xs, qw["W13"], qw["W13_s"],
+                                            moe.MOE_EPI_SWIGLU_QUANT, hq, hs, mx=mx)
+        elif mx:
+            moe.moe_grouped_gemm_mxfp8(E + 1, offs, R, 2 * I, H, aq, as_, qw["W13"], qw["W13_s"],
+                                       moe.MOE_EPI_SWIGLU_QUANT, hq, hs)
+        else:
+            moe.moe_grouped_gemm_fp8(E + 1, offs, R, 2 * I, H, aq, as_, qw["W13"], qw["W13_s"],
+                                     moe.MOE_EPI_SWIGLU_QUANT, hq, hs, None)
+        torch.cuda.synchronize()
+        outs.append((to_host(hq), to_host(hs)))
+    assert moe.moe_device_error() == 0
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+    unclaimed = to_host(perm_tok) < 0
+    assert unclaimed.sum() == 2 and not outs[1][0][unclaimed].any()
