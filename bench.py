@@ -30,7 +30,8 @@ from fp8_gemm_sigmoid_b300 import moe, replicas, synthetic as sy  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gate": "gate.cu",
-                  "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu"}
+                  "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu",
+                  "mx/gemm1_swiglu": "gemm_mx.cu", "mx/gemm2_down": "gemm_mx.cu"}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 STAGED_SECONDS = 2.5  # the per-stage pass runs at least this long (>= 20 clock samples)
 
@@ -276,29 +277,71 @@ def stage_work(cfg):
     }
 
 
+def source_digest(name):
+    """SHA-256 over a kernel source file of csrc/ and every file it includes with quotes,
+    transitively, in first-inclusion order: any edit to the code the kernel is built from
+    changes it."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    seen = []
+
+    def walk(path):
+        path = os.path.normpath(path)
+        if path in seen:
+            return
+        seen.append(path)
+        with open(path, "rb") as f:
+            text = f.read()
+        h.update(text)
+        for inc in re.findall(rb'^\s*#\s*include\s+"([^"]+)"', text, re.M):
+            walk(os.path.join(os.path.dirname(path), inc.decode()))
+
+    walk(os.path.join(ROOT, "fp8_gemm_sigmoid_b300", "csrc", name))
+    return h.hexdigest()
+
+
 def measured_traffic(stage, cfg):
     """DRAM bytes (read + write) of one launch of the stage's kernel on cfg's workload, from the
     ncu counters recorded in profiles/dram_traffic.txt, or (None, None) when no capture of the
     kernel's current source exists.  A capture is taken on a cut-down case of the workload's
     shape (fewer tokens and experts, the same rows per expert); its bytes scale to cfg's
-    workload by the tokens processed.  Each line of the file records the SHA-256 of the
-    kernel's source at capture time, and a line only counts while the source is unchanged."""
-    import hashlib
+    workload by the tokens processed.  Each line of the file records source_digest() of the
+    kernel's source at capture time, and a line only counts while that digest is unchanged.
+    The gate's bytes (the tokens, their T x K outputs and the [E, H] gate weight) scale by the
+    tokens at the same E, so its capture keeps the experts instead.
+    Power-of-two (MXFP8) stages are recorded as mx/<stage>."""
+    if cfg.get("mode") == "mxfp8" and stage.startswith("gemm"):
+        stage = "mx/" + stage
     src = KERNEL_SOURCES.get(stage)
     if src is None or not os.path.exists(TRAFFIC_FILE):
         return None, None
-    with open(os.path.join(ROOT, "fp8_gemm_sigmoid_b300", "csrc", src), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+    sha = source_digest(src)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
             if line.startswith("#") or len(parts) < 7:
                 continue
             workload, st, digest, rd, wr, cap_T, cap_E = parts[:7]
-            if workload == cfg["name"] and st == stage and digest == sha and int(cap_E) * cfg["T"] == int(cap_T) * cfg["n_experts"]:
+            same_shape = int(cap_E) * cfg["T"] == int(cap_T) * cfg["n_experts"]
+            if stage == "gate":  # x, the T x K outputs and the [E, H] gate weight: same E, any T
+                same_shape = int(cap_E) == cfg["n_experts"]
+            if workload == cfg["name"] and st == stage and digest == sha and same_shape:
                 scale = cfg["T"] / int(cap_T)
                 return int(round((int(rd) + int(wr)) * scale)), "ncu capture at T=%s E=%s scaled by tokens x%.3g" % (cap_T, cap_E, scale)
     return None, None
+
+
+def tensor_peak(peaks, clk):
+    """FP8 tensor peak for a kernel timed in a region with clock record clk: the measured
+    BF16 burst figure x 2, or the sustained (seconds-long, power-capped) figure x 2 when the
+    region's median SM clock sat below 95 % of its maximum with sw_power_cap active -- the
+    regime the sustained figure was measured in.  Returns (peak TFLOP/s, regime label)."""
+    if clk and clk.get("samples", 0) >= 5 and "sw_power_cap" in clk.get("reasons", ()) and \
+            clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"]:
+        return peaks["bf16_sus"] * FP8_PER_BF16, "sustained (power-capped region, %.0f of %.0f MHz)" % (
+            clk["sm_mhz"], clk["sm_max_mhz"])
+    return peaks["bf16"] * FP8_PER_BF16, "burst"
 
 
 def barrier_sync(dist_on):
@@ -687,9 +730,9 @@ def main():
     stage_clk = clocks.stats(*r2)
 
     work = stage_work(cfg)
-    # the grouped GEMMs are timed in short regions at full clock: their denominator is the
-    # burst BF16 figure times the nominal FP8:BF16 ratio
-    fp8_peak = peaks["bf16"] * FP8_PER_BF16
+    # the grouped GEMMs' denominator: the BF16 figure of the regime their timed region ran in
+    # (burst, or sustained when the clocks show the power cap) times the nominal FP8:BF16 ratio
+    fp8_peak, regime = tensor_peak(peaks, stage_clk)
     stages = {}
     for s in Layer.STAGES:
         if s == "bias_update" and not cfg["update_bias"]:
@@ -708,8 +751,9 @@ def main():
     if kind == "tensor":
         roof = {"kernel": dom, "bound": "tensor", "achieved": amount / dom_t / 1e12, "peak": fp8_peak,
                 "unit": "TFLOP/s",
-                "peak_source": "%s bf16 burst x %.0f (nominal FP8:BF16), of %s" % (
-                    peaks["src"], FP8_PER_BF16, peaks["src"])}
+                "peak_source": "%s bf16 %s x %.0f (nominal FP8:BF16), of %s" % (
+                    peaks["src"], regime, FP8_PER_BF16, peaks["src"]),
+                "frac_of_burst": amount / dom_t / 1e12 / (peaks["bf16"] * FP8_PER_BF16)}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": amount / dom_t / 1e9, "peak": peaks["hbm"],
                 "unit": "GB/s", "peak_source": "%s copy bandwidth" % peaks["src"]}

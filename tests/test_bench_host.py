@@ -29,9 +29,23 @@ def test_stage_work_matches_the_layer_closed_forms():
 
 
 def _sha(stage):
-    path = os.path.join(bench.ROOT, "fp8_gemm_sigmoid_b300", "csrc", bench.KERNEL_SOURCES[stage])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    return bench.source_digest(bench.KERNEL_SOURCES[stage])
+
+
+def test_source_digest_covers_the_included_headers(tmp_path, monkeypatch):
+    csrc = tmp_path / "fp8_gemm_sigmoid_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
+    (csrc / "k.cu").write_text('#include "a.cuh"\n#include <stdio.h>\nkernel\n')
+    (csrc / "a.cuh").write_text('#include "../../include/api.h"\n#include "k.cu"\n')
+    (tmp_path / "include" / "api.h").write_text("v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d1 = bench.source_digest("k.cu")
+    (tmp_path / "include" / "api.h").write_text("v2\n")   # two includes down
+    d2 = bench.source_digest("k.cu")
+    assert d1 != d2
+    whole = hashlib.sha256((csrc / "k.cu").read_bytes() + (csrc / "a.cuh").read_bytes() + b"v2\n")
+    assert d2 == whole.hexdigest()   # each file once, in first-inclusion order
 
 
 def test_measured_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch):
@@ -39,15 +53,22 @@ def test_measured_traffic_is_reported_only_for_the_measured_source(tmp_path, mon
     # full workload by the tokens processed
     f = tmp_path / "traffic.txt"
     f.write_text("# workload stage sha read write T E\n"
-                 "v3_prefill gate %s 1000 24 2048 32\n"
+                 "v3_prefill gate %s 1000 24 2048 256\n"
                  "v3_prefill combine %s 7 8 2048 32\n"
-                 "v3_prefill quant %s 7 8 2048 64\n" % (_sha("gate"), "0" * 64, _sha("quant")))
+                 "v3_prefill quant %s 7 8 2048 64\n"
+                 "v3_prefill permute %s 100 28 2048 32\n"
+                 "v3_prefill mx/gemm1_swiglu %s 500 12 2048 32\n"
+                 % (_sha("gate"), "0" * 64, _sha("quant"), _sha("permute"), _sha("mx/gemm1_swiglu")))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     full = sy.config("v3_prefill")
-    assert bench.measured_traffic("gate", full)[0] == 1024 * 8
-    assert bench.measured_traffic("gate", sy.config("v3_prefill", T=2048, n_experts=32))[0] == 1024
+    assert bench.measured_traffic("gate", full)[0] == 1024 * 8       # the gate keeps E, scales by T
+    assert bench.measured_traffic("gate", sy.config("v3_prefill", T=2048))[0] == 1024
+    assert bench.measured_traffic("gate", sy.config("v3_prefill", T=2048, n_experts=32)) == (None, None)
+    assert bench.measured_traffic("permute", full)[0] == 128 * 8      # same rows per expert
     assert bench.measured_traffic("combine", full) == (None, None)   # source changed since
     assert bench.measured_traffic("quant", full) == (None, None)     # another rows-per-expert shape
+    assert bench.measured_traffic("gemm1_swiglu", full) == (None, None)   # only the MX kernel captured
+    assert bench.measured_traffic("gemm1_swiglu", dict(full, mode="mxfp8"))[0] == 512 * 8
     assert bench.measured_traffic("gate", sy.config("v3_decode")) == (None, None)  # other workload
     assert bench.measured_traffic("bias_update", full) == (None, None)
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
@@ -68,3 +89,16 @@ def test_gemm_rows_counts_whole_tiles():
     assert r["useful"] == 0 + 1 + 128 + 129 + 256 + 300
     assert r["tile_rows"] == (0 + 1 + 1 + 2 + 2 + 3) * 128
     assert r["tile_efficiency"] == r["useful"] / r["tile_rows"]
+
+
+def test_tensor_peak_follows_the_clock_regime():
+    peaks = dict(bf16=1747.0, bf16_sus=1378.6, hbm=6494.3, src="measured")
+    burst = bench.tensor_peak(peaks, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "samples": 40, "reasons": []})
+    assert burst == (1747.0 * 2, "burst")
+    capped = {"sm_mhz": 1440.0, "sm_max_mhz": 2032.0, "samples": 51, "reasons": ["sw_power_cap"]}
+    peak, label = bench.tensor_peak(peaks, capped)
+    assert peak == 1378.6 * 2 and label.startswith("sustained")
+    # too few samples, or full clock despite the flag, or no record: the burst figure
+    assert bench.tensor_peak(peaks, dict(capped, samples=3))[1] == "burst"
+    assert bench.tensor_peak(peaks, dict(capped, sm_mhz=2010.0))[1] == "burst"
+    assert bench.tensor_peak(peaks, None)[1] == "burst"
