@@ -1,6 +1,10 @@
 """Build libmoe.so (the C-ABI CUDA library) in-tree with nvcc for sm_103a.
 
-Usage: python -m fp8_gemm_sigmoid_b300.build [--force] [--verbose]
+Usage: python -m fp8_gemm_sigmoid_b300.build [--force] [--verbose] [--checks]
+
+--checks builds libmoe_checks.so instead: the same sources with -DMOE_CHECKS, whose kernels
+check the indices callers pass in and record failures in the device error word (a debug
+build; the hot path is libmoe.so).
 """
 import glob
 import os
@@ -11,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe.so")
+CHECKS_LIB = os.path.join(HERE, "libmoe_checks.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 NVCC_FLAGS = [
@@ -31,24 +36,27 @@ def _deps():
                               [os.path.join(ROOT, "include", "moe.h")])
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force=False, verbose=False):
-    """Compile every .cu under csrc/ into libmoe.so (one nvcc call per object, then link)."""
-    if not force and up_to_date():
-        return LIB
-    objdir = os.path.join(HERE, "_build")
+def build(force=False, verbose=False, checks=False):
+    """Compile every .cu under csrc/ into libmoe.so, or with checks=True into
+    libmoe_checks.so with -DMOE_CHECKS (one nvcc call per object, then link)."""
+    lib = CHECKS_LIB if checks else LIB
+    if not force and up_to_date(lib):
+        return lib
+    objdir = os.path.join(HERE, "_build_checks" if checks else "_build")
     os.makedirs(objdir, exist_ok=True)
     objs = []
     procs = []
     for src in sources():
         obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
-        cmd = [NVCC, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+        cmd = [NVCC, *NVCC_FLAGS, *(["-DMOE_CHECKS"] if checks else []), "-I", os.path.join(ROOT, "include"),
+               "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
             print(" ".join(cmd), flush=True)
@@ -64,14 +72,14 @@ def build(force=False, verbose=False):
             sys.stdout.write("nvcc failed on %s\n" % src)
     if failed:
         raise RuntimeError("libmoe build failed")
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     link = [NVCC, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "shared",
             "-Xlinker", "--no-undefined",
             *objs, "-o", tmp]
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv, checks="--checks" in sys.argv))

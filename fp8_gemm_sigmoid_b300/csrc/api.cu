@@ -106,11 +106,13 @@ extern "C" moe_status moe_device_error(int32_t* code) {
     MOE_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
     const int zero = 0;
     MOE_CUDA_CHECK(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
-    int32_t tc = 0, mx = 0, gate = 0;
+    int32_t tc = 0, mx = 0, gate = 0, perm = 0, comb = 0;
     MOE_TRY(tc_read_and_clear_error(&tc));
     MOE_TRY(mx_read_and_clear_error(&mx));
     MOE_TRY(gate_read_and_clear_error(&gate));
-    *code = v ? v : (tc ? tc : (mx ? mx : gate));
+    MOE_TRY(permute_read_and_clear_check(&perm));
+    MOE_TRY(combine_read_and_clear_check(&comb));
+    *code = v ? v : (tc ? tc : (mx ? mx : (gate ? gate : (perm ? perm : comb))));
     return MOE_OK;
 }
 

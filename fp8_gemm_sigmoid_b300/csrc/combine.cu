@@ -11,6 +11,16 @@
 #include "internal.h"
 
 namespace moe {
+
+// Check word of the MOE_CHECKS build (0 = none): 0x302, a combine row outside [-1, T*K)
+// (-1 marks a dropped slot); 0x303, a gathered row index past the source rows.
+__device__ int g_combine_check = 0;
+
+moe_status combine_read_and_clear_check(int32_t* code) {
+    MOE_CUDA_CHECK(read_and_clear_word(g_combine_check, code));
+    return MOE_OK;
+}
+
 namespace {
 
 // One thread per (token, 8 BF16 columns): 16-byte gathered loads, 16-byte store.
@@ -29,7 +39,10 @@ combine_bf16_kernel(int64_t T, int H, int K, const uint16_t* __restrict__ yexp,
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
         for (int k = 0; k < K; ++k) {
             const int64_t r = row_of[t * K + k];
-            if (r < 0 || r >= T * K) continue;  // dropped slot
+            if (r < 0 || r >= T * K) {  // dropped slot (-1); anything else is a caller's error
+                (void)MOE_DCHECK(g_combine_check, r == -1, 0x302);
+                continue;
+            }
             const float wk = w[t * K + k];
             uint4 v = *reinterpret_cast<const uint4*>(yexp + r * H + ch * 8);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -72,7 +85,10 @@ combine_f32_kernel(int64_t T, int H, int K, const float* __restrict__ yexp,
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
             const int64_t r = row_of[t * K + k];
-            if (r < 0 || r >= T * K) continue;  // dropped slot
+            if (r < 0 || r >= T * K) {  // dropped slot (-1); anything else is a caller's error
+                (void)MOE_DCHECK(g_combine_check, r == -1, 0x302);
+                continue;
+            }
             const float wk = w[t * K + k];
             float4 v = *reinterpret_cast<const float4*>(yexp + r * H + ch * 4);
             acc.x = __fadd_rn(acc.x, __fmul_rn(wk, v.x));

@@ -26,9 +26,30 @@
         if (_s != MOE_OK) return _s;                                            \
     } while (0)
 
+// Device-side checks of the MOE_CHECKS build (a stand-in for a memory checker): a failed check
+// records its code in the translation unit's check word (the first failure wins) and the
+// caller skips the access instead of making it.  The default build compiles them away.
+#ifdef MOE_CHECKS
+#define MOE_DCHECK(word, cond, code) ((cond) ? true : (atomicCAS(&(word), 0, (code)), false))
+#else
+#define MOE_DCHECK(word, cond, code) (true)
+#endif
+
 namespace moe {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Reads a device word of this translation unit (an error or check word) and clears it.
+template <typename T>
+inline cudaError_t read_and_clear_word(const T& symbol, int32_t* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, symbol, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(symbol, &zero, sizeof(int));
+    *code = v;
+    return e;
+}
 
 // Host-side set-up that must run once on each device a process uses (kernel attributes such
 // as the dynamic shared-memory limit are per device).  Each call site owns one instance.

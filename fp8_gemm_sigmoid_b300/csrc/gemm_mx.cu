@@ -163,7 +163,7 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     tile_prefix<kThreads>(p, warp_sums, tile_start);
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = tile_start[p.n_groups];
+    const int total = offsets_usable<kThreads>(p, p.rows, &g_mx_error, 0x122) ? tile_start[p.n_groups] : 0;
 
     if (warp < kEpiWarp0) {
         // register split: 8 x 128 (producer, MMA, idle, scale writers) + 4 x 232 (epilogue)
@@ -182,7 +182,7 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
                 int32_t tok[4] = {0, 0, 0, 0};
                 if (p.gather)
-                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok);
+                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok, p.n_tok, &g_mx_error, 0x132);
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     bool w = true;
                     if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget);
@@ -269,7 +269,7 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 const float* ws1 = b1 < nbk ? p.Ws + (static_cast<int64_t>(c.g) * nbk + b1) * p.nkb : ws0;
                 const int r = c.row0 + q * 32 + lane;
                 // this row's scale column (K-block-major As) or, gathered, its token's Xs row
-                const float* as_col = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, 0)) * p.nkb
+                const float* as_col = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, p.n_tok, 0, &g_mx_error, 0x132)) * p.nkb
                                                : p.As + (r < c.row_end ? r : c.row0);
                 const int64_t kstep = p.gather ? 1 : p.rows;
                 for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += 4) {

@@ -116,11 +116,34 @@ __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* m
 }
 
 // Token of row r of a gathered A operand (rows [row0, row_end) of the tile's group): gather[r],
-// with rows past the group's end and unclaimed rows (index < 0) mapped to `none`.
-__device__ __forceinline__ int32_t gather_row(const int32_t* gather, int r, int row_end, int32_t none) {
+// with rows past the group's end, unclaimed rows (index -1) and indices past the n_tok tokens
+// mapped to `none`.  The MOE_CHECKS build records `code` in *word for an index that is
+// neither -1 nor a token.
+__device__ __forceinline__ int32_t gather_row(const int32_t* gather, int r, int row_end, int32_t n_tok,
+                                              int32_t none, int* word, int code) {
     if (r >= row_end) return none;
     const int32_t t = gather[r];
-    return t < 0 ? none : t;
+    if (t >= 0 && t < n_tok) return t;
+    (void)MOE_DCHECK(*word, t == -1, code);
+    (void)word; (void)code;
+    return none;
+}
+
+// MOE_CHECKS build: whether the groups' offsets are usable (offs[0] >= 0, non-decreasing,
+// offs[n_groups] <= rows), agreed by the whole CTA (kThreads threads, every one calls this).
+// A CTA that finds them unusable records `code` and runs no tile.
+template <int kThreads>
+__device__ bool offsets_usable(const Groups& p, int rows, int* word, int code) {
+    bool ok = true;
+#ifdef MOE_CHECKS
+    for (int g = threadIdx.x; g < p.n_groups; g += kThreads)
+        ok = ok && p.offs[g] >= 0 && p.offs[g] <= p.offs[g + 1] && p.offs[g + 1] <= rows;
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && threadIdx.x == 0) atomicCAS(word, 0, code);
+#else
+    (void)p; (void)rows; (void)word; (void)code;
+#endif
+    return ok;
 }
 
 // 2D TMA store of a [32 rows x 128 B] box from shared memory (128-byte swizzle) at (x, y).

@@ -165,7 +165,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     tile_prefix<kThreads>(p, warp_sums, tile_start);  // contains the CTA barriers that publish the set-up
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = tile_start[p.n_groups];
+    const int total = offsets_usable<kThreads>(p, p.rows, &g_tc_error, 0x121) ? tile_start[p.n_groups] : 0;
 
     if (warp < kEpiWarp0) {
         // register split: 4 x 48 (TMA, MMA, scale loader, idle) + 8 x 224 (epilogue) <= 12 x 168
@@ -184,7 +184,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int brow1 = c.g * p.N + b_block(p, c, 1) * 128;
                 int32_t tok[4] = {0, 0, 0, 0};
                 if (p.gather)
-                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok);
+                    for (int j = 0; j < 4; ++j) tok[j] = gather_row(p.gather, c.row0 + 4 * lane + j, c.row_end, p.n_tok, p.n_tok, &g_tc_error, 0x131);
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     bool w = true;
                     if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitBudget);
@@ -275,7 +275,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int r = c.row0 + lane + 32 * j;
-                    src[j] = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, 0)) * p.nkb
+                    src[j] = p.gather ? p.As + static_cast<int64_t>(gather_row(p.gather, r, c.row_end, p.n_tok, 0, &g_tc_error, 0x131)) * p.nkb
                                       : p.As + (r < c.row_end ? r : c.row0);
                 }
                 const int64_t kstep = p.gather ? 1 : p.rows;

@@ -35,5 +35,7 @@ moe_status launch_gate(const moe_config& c, int64_t T, const void* x, const void
                        float* logits_scratch, cudaStream_t s);
 size_t gate_scratch_bytes(const moe_config& c, int64_t T);
 moe_status gate_read_and_clear_error(int32_t* code);
+moe_status permute_read_and_clear_check(int32_t* code);   // MOE_CHECKS build: 0x301
+moe_status combine_read_and_clear_check(int32_t* code);   // MOE_CHECKS build: 0x302
 
 }  // namespace moe

@@ -22,6 +22,15 @@
 #include "internal.h"
 
 namespace moe {
+
+// Check word of the MOE_CHECKS build (0 = none): 0x301, a position outside the rows.
+__device__ int g_permute_check = 0;
+
+moe_status permute_read_and_clear_check(int32_t* code) {
+    MOE_CUDA_CHECK(read_and_clear_word(g_permute_check, code));
+    return MOE_OK;
+}
+
 namespace {
 
 constexpr int kChunk = 64;  // tokens per chunk
@@ -170,8 +179,10 @@ positions_match_kernel(int64_t T, int K, int E, int has_shared, const int32_t* _
         if (e >= 0) {
             const int32_t pos = wcnt[ew * E + e] + __popc(m & lt);
             const int64_t tt = t0 + i / K;
-            perm_tok[pos] = static_cast<int32_t>(tt);
-            row_of[t0 * K + i] = pos;
+            if (MOE_DCHECK(g_permute_check, pos >= 0 && pos < T * K, 0x301)) {
+                perm_tok[pos] = static_cast<int32_t>(tt);
+                row_of[t0 * K + i] = pos;
+            }
         } else if (i < n) {
             row_of[t0 * K + i] = -1;  // dropped slot: no row
         }
@@ -201,8 +212,10 @@ positions_kernel(int64_t T, int K, int E, int has_shared, const int32_t* __restr
         for (int tt = 0; tt < nt; ++tt)
             for (int k = 0; k < K; ++k)
                 if (sidx[tt * K + k] == e) {
-                    perm_tok[pos] = static_cast<int32_t>(t0 + tt);
-                    row_of[(t0 + tt) * K + k] = pos;
+                    if (MOE_DCHECK(g_permute_check, pos >= 0 && pos < T * K, 0x301)) {
+                        perm_tok[pos] = static_cast<int32_t>(t0 + tt);
+                        row_of[(t0 + tt) * K + k] = pos;
+                    }
                     ++pos;
                 }
     }
@@ -242,6 +255,7 @@ gather_tokens_kernel(int64_t T, int K, int E, int has_shared, int64_t row_bytes,
             for (int k = 0; k < K + has_shared; ++k) {
                 const int64_t r = k < K ? __shfl_sync(0xffffffffu, my_row, k) : T * K + t;
                 if (r < 0) continue;
+                if (!MOE_DCHECK(g_permute_check, r < T * K + (has_shared ? T : 0), 0x301)) continue;
                 uint4* d4 = reinterpret_cast<uint4*>(dst + r * row_bytes);
 #pragma unroll
                 for (int j = 0; j < kGatherPiece; ++j) {

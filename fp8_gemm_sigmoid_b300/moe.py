@@ -6,6 +6,7 @@ torch stream, and raises MoEError on a non-OK status.  All arithmetic runs in li
 CUDA kernels; if the library is missing this module raises instead of computing anything
 another way.
 """
+import contextlib
 import ctypes
 import os
 
@@ -13,6 +14,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
+CHECKS_LIB_PATH = os.path.join(_HERE, "libmoe_checks.so")  # the -DMOE_CHECKS debug build
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
 MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8 = 0, 1, 2
@@ -76,21 +78,44 @@ _SIGS = {
 }
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run `python -m fp8_gemm_sigmoid_b300.build%s`"
+                           % (path, " --checks" if path == CHECKS_LIB_PATH else ""))
+    L = ctypes.CDLL(path)
+    L.moe_status_string.argtypes = [ctypes.c_int]
+    L.moe_status_string.restype = ctypes.c_char_p
+    for name, args in _SIGS.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    return L
+
+
 def _lib_handle():
     global _L
     if _L is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libmoe.so is not built (%s); run `python -m "
-                               "fp8_gemm_sigmoid_b300.build`" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        L.moe_status_string.argtypes = [ctypes.c_int]
-        L.moe_status_string.restype = ctypes.c_char_p
-        for name, args in _SIGS.items():
-            f = getattr(L, name)
-            f.argtypes = args
-            f.restype = ctypes.c_int
-        _L = L
+        _L = _load(LIB_PATH)
     return _L
+
+
+_CHECKS = None
+
+
+@contextlib.contextmanager
+def checks_library():
+    """Routes this module's calls to libmoe_checks.so (the same kernels with the MOE_CHECKS
+    index checks compiled in) inside the with-block, then back to libmoe.so.  Both libraries
+    stay loaded side by side; each has its own device error words."""
+    global _L, _CHECKS
+    if _CHECKS is None:
+        _CHECKS = _load(CHECKS_LIB_PATH)
+    prev = _lib_handle()
+    _L = _CHECKS
+    try:
+        yield _CHECKS
+    finally:
+        _L = prev
 
 
 def exported_symbols():

@@ -359,7 +359,21 @@ MOE_API moe_status moe_logfmt_decode(int32_t n_bits, int64_t rows, int64_t cols,
                                      moe_stream_t stream);
 
 /* Device-side error word written by bounded waits inside the kernels (0 = none).  Reading
- * it synchronises the device.  *code receives the word; the call then clears it. */
+ * it synchronises the device.  *code receives the word; the call then clears it.
+ *  Bounded waits: 0x101-0x104 (FP32-scale GEMM), 0x111-0x114 (power-of-two GEMM), gate
+ *  codes, 0x1ff (moe_selftest_wait_timeout).
+ *  libmoe_checks.so, the same sources built with -DMOE_CHECKS (no counterpart on the pages:
+ *  a debug build in place of a memory checker), also checks the indices that callers pass in
+ *  and the permutation's own positions; a failed check records its code and skips the access
+ *  (the first failure of a kind wins):
+ *   0x121 / 0x122  a grouped GEMM's offs not 0 <= offs[g] <= offs[g+1] <= rows (the CTA runs
+ *                  no tile); FP32-scale / power-of-two GEMM
+ *   0x131 / 0x132  a gathered GEMM's perm_tok entry neither -1 nor in [0, T) (read as a zero row)
+ *   0x301          a permutation position outside [0, T*K) (not reachable through the ABI)
+ *   0x302          a combine row_of entry neither -1 nor in [0, T*K) (the slot is skipped)
+ *  The default libmoe.so compiles these checks away.  It clamps the gathered GEMM's token
+ *  indices the same way, and the combine skips out-of-range rows, but a GEMM given unusable
+ *  offs reads and writes out of bounds. */
 MOE_API moe_status moe_device_error(int32_t* code);
 
 /* Self-test of the bounded-wait error path (no counterpart on the pages): one thread of a
