@@ -20,6 +20,7 @@ import sys
 import tempfile
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -275,6 +276,20 @@ def stage_work(cfg):
         "combine": ("hbm", R * H * 2 + T * H * 2 + T * K * 8),
         "bias_update": ("hbm", E * 12),
     }
+
+
+def gemm_bytes(cfg, counts):
+    """Algorithmic HBM bytes of each grouped GEMM: the FP8 weights and scales of every expert
+    that received a row (and of the shared expert), the A rows and scales read, and the output
+    written.  At small T (decode) these, not the FLOPs, bound the GEMMs."""
+    T, H, I, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["top_k"]
+    S = int(cfg["has_shared"])
+    R = T * K + T * S
+    n_w = int((np.asarray(counts) > 0).sum()) + S
+    w13 = n_w * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
+    w2 = n_w * (H * I + (H // 128) * (I // 128) * 4)
+    return {"gemm1_swiglu": w13 + R * (H + H // 128 * 4) + R * (I + I // 128 * 4),
+            "gemm2_down": w2 + R * (I + I // 128 * 4) + R * H * 2}
 
 
 def source_digest(name):
@@ -733,6 +748,7 @@ def main():
     # the grouped GEMMs' denominator: the BF16 figure of the regime their timed region ran in
     # (burst, or sustained when the clocks show the power cap) times the nominal FP8:BF16 ratio
     fp8_peak, regime = tensor_peak(peaks, stage_clk)
+    gbytes = gemm_bytes(cfg, counts)
     stages = {}
     for s in Layer.STAGES:
         if s == "bias_update" and not cfg["update_bias"]:
@@ -740,13 +756,20 @@ def main():
         kind, amount = work[s]
         t = stage_ms[s] / 1e3
         if kind == "tensor":
+            # a GEMM is bound by its FLOPs or by its bytes, whichever takes longer at peak
             ach = amount / t / 1e12 if t > 0 else None
-            stages[s] = {"ms": stage_ms[s], "TFLOP/s": ach, "frac_fp8_peak": ach / fp8_peak if ach else None}
+            gbs = gbytes[s] / t / 1e9 if t > 0 else None
+            bound = "tensor" if amount / (fp8_peak * 1e12) >= gbytes[s] / (peaks["hbm"] * 1e9) else "hbm"
+            stages[s] = {"ms": stage_ms[s], "bound": bound, "TFLOP/s": ach,
+                         "frac_fp8_peak": ach / fp8_peak if ach else None,
+                         "GB/s": gbs, "frac_hbm": gbs / peaks["hbm"] if gbs else None}
         else:
             ach = amount / t / 1e9 if t > 0 else None
             stages[s] = {"ms": stage_ms[s], "GB/s": ach, "frac_hbm": ach / peaks["hbm"] if ach else None}
     dom = max(stages, key=lambda s: stages[s]["ms"])
     kind, amount = work[dom]
+    if kind == "tensor" and stages[dom]["bound"] == "hbm":
+        kind, amount = "hbm", gbytes[dom]
     dom_t = stage_ms[dom] / 1e3
     if kind == "tensor":
         roof = {"kernel": dom, "bound": "tensor", "achieved": amount / dom_t / 1e12, "peak": fp8_peak,

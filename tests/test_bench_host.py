@@ -4,6 +4,8 @@ measured on.  CPU only."""
 import hashlib
 import os
 
+import numpy as np
+
 import bench
 from fp8_gemm_sigmoid_b300 import synthetic as sy
 
@@ -102,3 +104,25 @@ def test_tensor_peak_follows_the_clock_regime():
     assert bench.tensor_peak(peaks, dict(capped, samples=3))[1] == "burst"
     assert bench.tensor_peak(peaks, dict(capped, sm_mhz=2010.0))[1] == "burst"
     assert bench.tensor_peak(peaks, None)[1] == "burst"
+
+
+def test_gemm_bytes_count_the_hit_experts_once():
+    cfg = sy.config("v3_decode")
+    T, H, I, K = cfg["T"], cfg["hidden"], cfg["inter"], cfg["top_k"]
+    R = T * K + T
+    counts = np.zeros(cfg["n_experts"], np.int64)
+    counts[[3, 7]] = [T * K - 5, 5]                 # two experts hit, plus the shared one
+    b = bench.gemm_bytes(cfg, counts)
+    w13 = 3 * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
+    assert b["gemm1_swiglu"] == w13 + R * (H + H // 128 * 4) + R * (I + I // 128 * 4)
+    w2 = 3 * (H * I + (H // 128) * (I // 128) * 4)
+    assert b["gemm2_down"] == w2 + R * (I + I // 128 * 4) + R * H * 2
+    # decode with every expert hit streams 11.3 GB of FP8 weights: HBM-bound, not tensor-bound
+    full = bench.gemm_bytes(cfg, np.ones(cfg["n_experts"]))
+    peaks = dict(bf16=1747.0, bf16_sus=1378.6, hbm=6494.3)
+    flops = bench.stage_work(cfg)["gemm1_swiglu"][1]
+    assert full["gemm1_swiglu"] / (peaks["hbm"] * 1e9) > flops / (2 * peaks["bf16"] * 1e12)
+    prefill = sy.config("v3_prefill")
+    pb = bench.gemm_bytes(prefill, np.ones(prefill["n_experts"]))
+    assert pb["gemm1_swiglu"] / (peaks["hbm"] * 1e9) < bench.stage_work(prefill)["gemm1_swiglu"][1] / (
+        2 * peaks["bf16"] * 1e12)
