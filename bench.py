@@ -30,7 +30,7 @@ from fp8_gemm_sigmoid_b300 import moe, replicas, synthetic as sy  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gate": "gate.cu",
+KERNEL_SOURCES = {"gemm1_swiglu": "gemm_tc.cu", "gemm2_down": "gemm_tc.cu", "gate": "gate.cu", "gate_quant": "gate.cu",
                   "quant": "quant.cu", "permute": "permute.cu", "combine": "combine.cu",
                   "mx/gemm1_swiglu": "gemm_mx.cu", "mx/gemm2_down": "gemm_mx.cu"}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
@@ -39,7 +39,7 @@ STAGED_SECONDS = 2.5  # the per-stage pass runs at least this long (>= 20 clock 
 # kernels each entry point launches in the FP8 layer (memsets excluded); summed into
 # gpu_launches.  moe_permute: chunk histogram, scan, positions, row gather, scale gather.
 # Each grouped GEMM is one persistent kernel (its tile schedule is built in shared memory).
-LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_permute": 5,
+LAUNCHES = {"moe_gate": 1, "moe_quant_1x128": 1, "moe_gate_quant": 1, "moe_permute": 5,
             "moe_grouped_gemm_fp8/swiglu": 1, "moe_grouped_gemm_fp8/store": 1,
             "moe_combine": 1, "moe_bias_update": 1}
 
@@ -197,6 +197,18 @@ class Layer:
         self.hq = torch.empty(R, I, dtype=u8, device=dev)
         self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)  # K-block-major
         self.yexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        # FP8 modes: the gate quantises x in the same pass when its tensor-core kernel takes the
+        # shape (moe_forward then launches no separate quantiser); the staged pass does the same
+        self.fused = False
+        try:
+            o = self.out
+            moe.moe_gate_quant(cfg, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"],
+                               self.xq, self.xs)
+            self.fused = True
+        except moe.MoEError as e:
+            if e.status != moe.MOE_ERR_UNSUPPORTED:
+                raise
+        self.stages = (["gate_quant"] if self.fused else ["gate", "quant"]) + Layer.STAGES[2:]
 
     def forward(self, world=1):
         """One layer step.  Under N > 1 token replicas the top-1 bias update runs after an
@@ -214,38 +226,45 @@ class Layer:
     STAGES = ["gate", "quant", "permute", "gemm1_swiglu", "gemm2_down", "combine", "bias_update"]
 
     def staged(self, ev, world=1):
-        """The same layer through the individual entry points, an event after each stage."""
+        """The same layer through the individual entry points, an event before the first stage
+        and after each of self.stages (len(self.stages) + 1 events)."""
         c, o = self.cfg, self.out
         T, H, I, E = c["T"], c["hidden"], c["inter"], c["n_experts"]
         G = E + int(c["has_shared"])
-        ev[0].record()
-        moe.moe_gate(c, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"])
-        ev[1].record()
-        if self.mx:
-            moe.moe_quant_1x128_pow2(self.x, self.xq, self.xs)
+        ev = iter(ev)
+        next(ev).record()
+        if self.fused:
+            moe.moe_gate_quant(c, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"],
+                               self.xq, self.xs)
+            next(ev).record()
         else:
-            moe.moe_quant_1x128(self.x, self.xq, self.xs)
-        ev[2].record()
+            moe.moe_gate(c, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"])
+            next(ev).record()
+            if self.mx:
+                moe.moe_quant_1x128_pow2(self.x, self.xq, self.xs)
+            else:
+                moe.moe_quant_1x128(self.x, self.xq, self.xs)
+            next(ev).record()
         moe.moe_permute(c, T, o["topk_idx"], o["counts"], self.xq, self.xs, self.offs, self.perm_tok,
                         self.row_of, self.aq, self.as_, self.ws)
-        ev[3].record()
+        next(ev).record()
         if self.mx:
             moe.moe_grouped_gemm_mxfp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
                                        self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs)
         else:
             moe.moe_grouped_gemm_fp8(G, self.offs, self.R, 2 * I, H, self.aq, self.as_, self.q["W13"],
                                      self.q["W13_s"], moe.MOE_EPI_SWIGLU_QUANT, self.hq, self.hs, self.ws)
-        ev[4].record()
+        next(ev).record()
         if self.mx:
             moe.moe_grouped_gemm_mxfp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
                                        self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None)
         else:
             moe.moe_grouped_gemm_fp8(G, self.offs, self.R, H, I, self.hq, self.hs, self.q["W2"],
                                      self.q["W2_s"], moe.MOE_EPI_STORE, self.yexp, None, self.ws)
-        ev[5].record()
+        next(ev).record()
         ysh = self.yexp[T * c["top_k"]:] if c["has_shared"] else None
         moe.moe_combine(c, T, self.yexp, self.row_of, o["topk_w"], ysh, self.y)
-        ev[6].record()
+        next(ev).record()
         if c["update_bias"]:
             if world > 1:  # token replicas: the update from the whole batch's histogram
                 replicas.global_bias_update(c, o["counts"], T, self.bias,
@@ -253,12 +272,12 @@ class Layer:
                                             T_global=world * T)
             else:
                 moe.moe_bias_update(c, T, o["counts"], self.bias)
-        ev[7].record()
+        next(ev).record()
 
     def launches_per_step(self):
-        n = sum(LAUNCHES[k] for k in ("moe_gate", "moe_quant_1x128", "moe_permute",
-                                      "moe_grouped_gemm_fp8/swiglu", "moe_grouped_gemm_fp8/store",
-                                      "moe_combine"))
+        first = ("moe_gate_quant",) if self.fused else ("moe_gate", "moe_quant_1x128")
+        n = sum(LAUNCHES[k] for k in first + ("moe_permute", "moe_grouped_gemm_fp8/swiglu",
+                                              "moe_grouped_gemm_fp8/store", "moe_combine"))
         return n + (LAUNCHES["moe_bias_update"] if self.cfg["update_bias"] else 0)
 
 
@@ -270,6 +289,8 @@ def stage_work(cfg):
     return {
         "gate": ("hbm", T * H * 2 + E * H * 2 + T * K * 8 + E * 4),
         "quant": ("hbm", T * H * 2 + T * H + T * (H // 128) * 4),
+        # the gate with the quantisation fused in: x read once, the codes and scales written
+        "gate_quant": ("hbm", T * H * 2 + E * H * 2 + T * K * 8 + E * 4 + T * H + T * (H // 128) * 4),
         "permute": ("hbm", T * K * 4 * 3 + R * (H + H // 128 * 4) + T * (H + H // 128 * 4)),
         "gemm1_swiglu": ("tensor", 2 * R * H * 2 * I),
         "gemm2_down": ("tensor", 2 * R * I * H),
@@ -339,7 +360,7 @@ def measured_traffic(stage, cfg):
                 continue
             workload, st, digest, rd, wr, cap_T, cap_E = parts[:7]
             same_shape = int(cap_E) * cfg["T"] == int(cap_T) * cfg["n_experts"]
-            if stage == "gate":  # x, the T x K outputs and the [E, H] gate weight: same E, any T
+            if stage in ("gate", "gate_quant"):  # x, the T x K outputs, the [E, H] gate weight: same E, any T
                 same_shape = int(cap_E) == cfg["n_experts"]
             if workload == cfg["name"] and st == stage and digest == sha and same_shape:
                 scale = cfg["T"] / int(cap_T)
@@ -608,7 +629,7 @@ def main():
     # warm-up (W whole-layer steps through moe_forward and through the staged calls)
     for _ in range(max(args.warmup, 3)):
         layer.forward(world)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(layer.stages) + 1)]
     for _ in range(2):
         layer.staged(ev, world)
     barrier_sync(dist_on)
@@ -634,16 +655,16 @@ def main():
     step_s = ms / args.steps / 1e3
     n_staged = max(args.steps, min(2000, int(args.staged_seconds / max(step_s, 1e-6)) + 1)
                    if args.staged_seconds > 0 else args.steps)
-    stage_ms = {s: 0.0 for s in Layer.STAGES}
+    stage_ms = {s: 0.0 for s in layer.stages}
     barrier_sync(dist_on)
-    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_staged)]
+    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(layer.stages) + 1)] for _ in range(n_staged)]
     r2 = [clocks.now()]
     for evs in all_evs:
         layer.staged(evs, world)
     barrier_sync(dist_on)
     r2.append(clocks.now())
     for evs in all_evs:
-        for i, s in enumerate(Layer.STAGES):
+        for i, s in enumerate(layer.stages):
             stage_ms[s] += evs[i].elapsed_time(evs[i + 1]) / n_staged
     counts = layer.out["counts"].cpu().numpy()
 
@@ -724,13 +745,14 @@ def main():
         b.record(stream)
         barrier_sync(dist_on)
         mx_value, mx_ms = replica_throughput(T, args.steps, a.elapsed_time(b), dist_on)
-        evs_mx = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+        evs_mx = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lmx.stages) + 1)] for _ in range(args.steps)]
         for evs in evs_mx:
             lmx.staged(evs, world)
         barrier_sync(dist_on)
         assert moe.moe_device_error() == 0
-        g1 = sum(evs[3].elapsed_time(evs[4]) for evs in evs_mx) / args.steps
-        g2 = sum(evs[4].elapsed_time(evs[5]) for evs in evs_mx) / args.steps
+        k1 = lmx.stages.index("gemm1_swiglu")
+        g1 = sum(evs[k1].elapsed_time(evs[k1 + 1]) for evs in evs_mx) / args.steps
+        g2 = sum(evs[k1 + 1].elapsed_time(evs[k1 + 2]) for evs in evs_mx) / args.steps
         w_mx = stage_work(cfg)
         mxfp8 = {"value": mx_value, "unit": "tokens/s", "ms_per_step": mx_ms / args.steps,
                  "gemm1_swiglu": {"ms": g1, "TFLOP/s": w_mx["gemm1_swiglu"][1] / g1 / 1e9,
@@ -750,7 +772,7 @@ def main():
     fp8_peak, regime = tensor_peak(peaks, stage_clk)
     gbytes = gemm_bytes(cfg, counts)
     stages = {}
-    for s in Layer.STAGES:
+    for s in layer.stages:
         if s == "bias_update" and not cfg["update_bias"]:
             continue
         kind, amount = work[s]

@@ -132,6 +132,16 @@ extern "C" moe_status moe_gate(const moe_config* cfg, int64_t T, const void* x, 
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" moe_status moe_gate_quant(const moe_config* cfg, int64_t T, const void* x, const void* Wg,
+                                     const float* bias, int32_t* topk_idx, float* topk_w,
+                                     int32_t* counts, uint8_t* xq, float* xs, moe_stream_t stream) {
+    if (!config_ok(cfg) || T < 0 || !counts) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !Wg || !bias || !topk_idx || !topk_w || !xq || !xs)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (T > INT64_MAX / cfg->hidden)) return MOE_ERR_INVALID_ARG;
+    return launch_gate_quant(*cfg, T, x, Wg, bias, topk_idx, topk_w, counts, xq, xs,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" moe_status moe_grouped_gemm_fp8(int32_t n_groups, const int32_t* offs, int64_t rows,
                                            int32_t N, int32_t Kdim, const uint8_t* A,
                                            const float* As, const uint8_t* W, const float* Ws,
@@ -215,19 +225,23 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
     void* gscratch = base + L.gemm_scratch;
     const size_t gbytes = L.total - L.gemm_scratch;
 
-    MOE_TRY(moe_gate(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, stream));
+    // FP8 modes: the gate also writes the 1x128 quantisation of x when its tensor-core kernel
+    // takes the shape (x is then read once); otherwise the quantiser runs on its own below
+    uint8_t* xq = fp8 ? reinterpret_cast<uint8_t*>(base + L.xq) : nullptr;
+    float* xs = fp8 ? reinterpret_cast<float*>(base + L.xs) : nullptr;
+    const bool fused = fp8 && gate_quant_supported(c) && aligned16(w->Wg);
+    if (fused) MOE_TRY(moe_gate_quant(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, xq, xs, stream));
+    else MOE_TRY(moe_gate(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, stream));
     if (update_bias) MOE_TRY(moe_bias_update(cfg, T, counts, bias, stream));
     if (T == 0) return MOE_OK;
     if (fp8) {
-        uint8_t* xq = reinterpret_cast<uint8_t*>(base + L.xq);
-        float* xs = reinterpret_cast<float*>(base + L.xs);
         uint8_t* aq = reinterpret_cast<uint8_t*>(base + L.aq);
         float* as = reinterpret_cast<float*>(base + L.as);
         uint8_t* hq = reinterpret_cast<uint8_t*>(base + L.hq);
         float* hs = reinterpret_cast<float*>(base + L.hs);
         void* yexp = base + L.yexp;
-        if (mx) MOE_TRY(moe_quant_1x128_pow2(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
-        else MOE_TRY(moe_quant_1x128(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
+        if (!fused && mx) MOE_TRY(moe_quant_1x128_pow2(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
+        else if (!fused) MOE_TRY(moe_quant_1x128(T, H, static_cast<const uint16_t*>(x), xq, xs, stream));
         // the permuted copy of the quantised rows: the grouped GEMM reads its A tiles with one TMA
         // box per K block (reading them straight from xq with tile::gather4, as
         // moe_grouped_gemm_fp8_gather does, measured twice as slow for the gate/up GEMM)

@@ -12,6 +12,10 @@
 //    accumulation), fed by TMA; then all 8 warps run the selection, two threads per token
 //    (each reads half of the token's groups from TMEM, the pair exchanges group scores and
 //    merges two local top-k lists through shared memory).  The kernel streams x once.
+//    With xq / xs given it also quantises x into 1x128 FP8 tiles (précis §3.2) while the
+//    tiles pass through shared memory for the MMA: four otherwise idle warps read each
+//    128-column block of their token row from the operand ring, so x is read from HBM once
+//    for the gate and the quantisation together.
 //  - gate_fused_kernel (FP32 inputs, or shapes outside the tensor-core kernel's range): the
 //    [kTok, E] logit tile is formed in shared memory on the CUDA cores, then each warp runs
 //    the selection for its tokens with warp shuffles (lane l holds experts l, l+32, ...).
@@ -19,6 +23,7 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "gemm_sched.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -224,8 +229,12 @@ constexpr int kGtMaxG = 8;
 constexpr int kGtABytes = kGtM * kGtK * 2;       // 16 KB
 constexpr int kGtBBytes = kGtMaxE * kGtK * 2;    // 32 KB (E rows)
 constexpr int kGtStageBytes = kGtABytes + kGtBBytes;
-constexpr int kGtSmem = kGtStages * kGtStageBytes + 4096;
+constexpr int kGqStageBytes = 32 * 128;    // one quantising warp's 32 rows x 128 codes
+constexpr int kGqOff = kGtStages * kGtStageBytes + 4096;  // 1024-aligned: the TMA store swizzle
+constexpr int kGtSmem = kGqOff + 4 * kGqStageBytes + 1024;
 constexpr long long kGtWaitBudget = 4000000000LL;
+constexpr int kGqWarp0 = 4;         // warps 4..7 quantise x (one token row per thread)
+constexpr int kGqWarps = 4;
 
 __device__ int g_gate_error = 0;
 
@@ -237,7 +246,73 @@ struct GateTcParams {
     int32_t* topk_idx;
     float* topk_w;
     int32_t* counts;
+    uint8_t* xq;      // [T, H] E4M3 codes, or nullptr (no quantisation)
+    float* xs;        // [T, H / 128] scales
+    int pow2;         // scales amax / 448 (0) or the power-of-two rule (1)
 };
+
+// Eight BF16 values (one 16-byte chunk) -> eight E4M3 codes, as quant_1x128_kernel codes them.
+template <bool kPow2>
+__device__ __forceinline__ uint2 code8(uint4 c, float mul, int e) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float f0 = __uint_as_float(w[k] << 16), f1 = __uint_as_float(w[k] & 0xffff0000u);
+        p[k] = kPow2 ? f32x2_to_e4m3x2(scale_pow2(f0, e), scale_pow2(f1, e))
+                     : f32x2_to_e4m3x2(__fmul_rn(f0, mul), __fmul_rn(f1, mul));
+    }
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// Quantises one 1x128 tile of a token row, exactly as quant_1x128_kernel does, from its two
+// 64-column halves in the operand ring (rows of 128 bytes, 16-byte chunk j at chunk position
+// j ^ r7, the 128-byte swizzle): its 128 codes to the 128-byte row `out` (16-byte chunk j at
+// chunk position j ^ r7 again) and its scale to *sc.
+__device__ __forceinline__ void quant_row_block(const uint8_t* half0, const uint8_t* half1, int r7, int pow2,
+                                                uint8_t* out, float* sc) {
+    const uint8_t* hp[2] = {half0, half1};
+    float amax = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 c = *reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4));
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+        }
+    if (amax == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(out + ((j ^ r7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        *sc = 1.f;
+        return;
+    }
+    if (pow2) {
+        const int e = pow2_exponent(amax);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const uint2 a = code8<true>(*reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4)), 0.f, e);
+                const uint2 b = code8<true>(*reinterpret_cast<const uint4*>(hp[h] + (((j + 1) ^ r7) << 4)), 0.f, e);
+                *reinterpret_cast<uint4*>(out + (((h * 4 + j / 2) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            }
+        *sc = exp2_int(e);
+    } else {
+        const float mul = __fdiv_rn(448.f, amax);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const uint2 a = code8<false>(*reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4)), mul, 0);
+                const uint2 b = code8<false>(*reinterpret_cast<const uint4*>(hp[h] + (((j + 1) ^ r7) << 4)), mul, 0);
+                *reinterpret_cast<uint4*>(out + (((h * 4 + j / 2) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            }
+        *sc = __fdiv_rn(amax, 448.f);
+    }
+}
 
 // sigmoid with the fast exponential and division intrinsics (a few ulp in FP32; the selection
 // is compared with the exact scores only where its margin exceeds 1e-5, and the weights within
@@ -253,7 +328,7 @@ __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f,
 
 __global__ void __launch_bounds__(kGtThreads, 1)
 gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-               const GateTcParams p) {
+               const __grid_constant__ CUtensorMap tmQ, const GateTcParams p) {
     using namespace sm100;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,10 +344,11 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int nk = p.H / kGtK;
     const uint32_t tmem_cols = 256;
+    const bool quant = p.xq != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGtStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 1 + (quant ? kGqWarps : 0));  // the MMA commit (+ the quantisers)
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
@@ -291,8 +367,10 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kGtM;
     // CTAs start their K sweep at different 64-column chunks so that concurrent loads of x
     // (128 B from each of 128 rows) spread over the memory channels instead of all CTAs
-    // hitting the same column offsets at once.  The sum order is fixed per CTA.
-    const int kc0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * 37) % nk);
+    // hitting the same column offsets at once.  The start is even, so that the two halves of
+    // each 128-column block arrive in consecutive stages (H % 128 == 0 when quantising).
+    // The sum order is fixed per CTA.
+    const int kc0 = 2 * static_cast<int>((static_cast<int64_t>(blockIdx.x) * 37) % (nk / 2 > 0 ? nk / 2 : 1)) % nk;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -344,6 +422,45 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             }
             mma_commit(acc_full);  // fires when every MMA above has completed
         }
+    } else if (quant && warp >= kGqWarp0 && warp < kGqWarp0 + kGqWarps) {
+        // 1x128 quantisation of x from the operand ring: thread r owns token row r of the
+        // tile.  Even stages hold the first half of a 128-column block and odd stages the
+        // second; once both have landed the block is coded from shared memory and both
+        // stages are released (the ring holds four).
+        // The codes go out through a per-warp staging box [32 rows][128 B] (the same 128-byte
+        // swizzle) by TMA stores, which clip the rows past T; the scales are stored directly.
+        const int r = (warp - kGqWarp0) * 32 + lane;
+        const int64_t t = t0 + r;
+        const int nb = p.H / 128;
+        uint8_t* stg = smem + kGqOff + (warp - kGqWarp0) * kGqStageBytes;
+        bool ok = true;
+        for (int it = 0; it + 1 < nk; it += 2) {  // stage it % kGtStages, phase parity (it / kGtStages) & 1
+            const int s = it % kGtStages, s1 = (it + 1) % kGtStages;
+            const uint32_t ph = (it / kGtStages) & 1u, ph1 = ((it + 1) / kGtStages) & 1u;
+            if (!mbar_wait(&full[s], ph, abort_flag, kGtWaitBudget) ||
+                !mbar_wait(&full[s1], ph1, abort_flag, kGtWaitBudget)) { ok = false; break; }
+            const int kb = ((it + kc0) % nk) / 2;
+            if (lane == 0) sched::tma_store_wait_read();  // the previous box has left the staging
+            __syncwarp();
+            float sc;
+            quant_row_block(smem + s * kGtStageBytes + r * 128, smem + s1 * kGtStageBytes + r * 128, r & 7,
+                            p.pow2, stg + lane * 128, &sc);
+            __syncwarp();
+            if (lane == 0) {  // this warp is done with both stages
+                mbar_arrive(&empty[s]);
+                mbar_arrive(&empty[s1]);
+            }
+            sched::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                sched::tma_store_2d(&tmQ, stg, kb * 128, static_cast<int32_t>(t0 + (warp - kGqWarp0) * 32));
+            if (t < p.T) p.xs[t * nb + kb] = sc;
+        }
+        if (lane == 0) sched::tma_store_wait_all();  // every code has reached global memory
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicCAS(&g_gate_error, 0, 0x204);
+        }
     }
     __syncwarp();  // the producer and MMA lanes rejoin their warps
     // ------------------------------------------------------------------ selection, all warps
@@ -356,6 +473,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         bool ok = mbar_wait(acc_full, 0, abort_flag, kGtWaitBudget);
         ok = __all_sync(0xffffffffu, ok);  // TMEM loads below are warp-collective
         tc_fence_after();
+        __syncthreads();  // the quantising warps have read the last stages: the ring is free
         if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicCAS(&g_gate_error, 0, 0x203);
@@ -475,10 +593,14 @@ bool gate_tc_supported(const moe_config& c) {
 }
 
 moe_status launch_gate_tc(const moe_config& c, int64_t T, const uint16_t* x, const uint16_t* Wg,
-                          const float* bias, int32_t* idx, float* w, int32_t* counts, cudaStream_t s) {
-    CUtensorMap tmX, tmW;
+                          const float* bias, int32_t* idx, float* w, int32_t* counts, cudaStream_t s,
+                          uint8_t* xq = nullptr, float* xs = nullptr) {
+    CUtensorMap tmX, tmW, tmQ;
     if (!make_tma_map_2d(&tmX, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, c.hidden, kGtM, kGtK))
         return MOE_ERR_CUDA;
+    if (xq && !make_tma_map_2d(&tmQ, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, c.hidden, 32, 128))
+        return MOE_ERR_CUDA;
+    if (!xq) tmQ = tmX;  // unused
     if (!make_tma_map_2d(&tmW, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.n_experts, c.hidden, c.n_experts, kGtK))
         return MOE_ERR_CUDA;
     static PerDeviceOnce attr_once;
@@ -486,8 +608,8 @@ moe_status launch_gate_tc(const moe_config& c, int64_t T, const uint16_t* x, con
         return cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
     }));
     GateTcParams p{T, c.hidden, c.n_experts, c.n_group, c.topk_group, c.top_k, c.routed_scaling_factor,
-                   bias, idx, w, counts};
-    gate_tc_kernel<<<static_cast<unsigned>(ceil_div(T, kGtM)), kGtThreads, kGtSmem, s>>>(tmX, tmW, p);
+                   bias, idx, w, counts, xq, xs, c.mode == MOE_MXFP8 ? 1 : 0};
+    gate_tc_kernel<<<static_cast<unsigned>(ceil_div(T, kGtM)), kGtThreads, kGtSmem, s>>>(tmX, tmW, tmQ, p);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
@@ -541,6 +663,21 @@ moe_status launch_gate(const moe_config& c, int64_t T, const void* x, const void
                               bias, idx, w, counts, s);
     return launch_typed(c, T, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
                         bias, idx, w, counts, s);
+}
+
+bool gate_quant_supported(const moe_config& c) {
+    return gate_tc_supported(c) && c.hidden % 128 == 0;
+}
+
+moe_status launch_gate_quant(const moe_config& c, int64_t T, const void* x, const void* Wg,
+                             const float* bias, int32_t* idx, float* w, int32_t* counts,
+                             uint8_t* xq, float* xs, cudaStream_t s) {
+    if (!gate_quant_supported(c) || !aligned16(x) || !aligned16(Wg) || !aligned16(xq))
+        return MOE_ERR_UNSUPPORTED;
+    MOE_CUDA_CHECK(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s));
+    if (T == 0) return MOE_OK;
+    return launch_gate_tc(c, T, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
+                          bias, idx, w, counts, s, xq, xs);
 }
 
 }  // namespace moe

@@ -30,6 +30,10 @@ size_t gemm_scratch_bytes(int32_t n_groups, int64_t rows, int32_t N, int32_t epi
 bool config_ok(const moe_config* c);
 
 // gate.cu
+bool gate_quant_supported(const moe_config& c);
+moe_status launch_gate_quant(const moe_config& c, int64_t T, const void* x, const void* Wg,
+                             const float* bias, int32_t* idx, float* w, int32_t* counts,
+                             uint8_t* xq, float* xs, cudaStream_t s);
 moe_status launch_gate(const moe_config& c, int64_t T, const void* x, const void* Wg,
                        const float* bias, int32_t* idx, float* w, int32_t* counts,
                        float* logits_scratch, cudaStream_t s);

@@ -16,8 +16,10 @@
 // 2^-(n-1)).  Decoding forms 2^(Step2 (K - 1)) from an exactly split exponent (integer part,
 // fraction, and the FMA residual of the product), times g1 = e^min computed once per tile,
 // a few 1e-7 off the exact value before its rounding to BF16.
-// One warp per tile, 4 values per lane (an 8-byte BF16 load); HBM-bound: 2 bytes read and
-// 1 (n <= 8) or 2 bytes written per value.
+// Eight lanes per tile, 16 values per lane (two 16-byte BF16 loads), so the tile's reductions
+// take three shuffle steps and its per-tile arithmetic is shared by 16 values; each lane takes
+// kTilesPerLane tiles per step with every load issued first.  2 bytes read and 1 (n <= 8) or
+// 2 bytes written per value.
 #include "common.cuh"
 
 namespace moe {
@@ -26,11 +28,19 @@ namespace {
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 constexpr float kLog2eLo = 1.925963033500011e-08f;  // log2(e) - kLog2e
-constexpr int kTilesInFlight = 4;  // tiles per warp and step, loaded together
+constexpr int kLanesPerTile = 8;
+constexpr int kTilesPerLane = 2;   // tiles per lane and step, loaded together
+constexpr int kTilesPerWarpStep = (32 / kLanesPerTile) * kTilesPerLane;
 
-__device__ __forceinline__ float warp_min(float v) {
+// max / min over the eight lanes of a tile group (lanes 8g .. 8g + 7)
+__device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = kLanesPerTile / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float group_min(float v) {
+#pragma unroll
+    for (int o = kLanesPerTile / 2; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
@@ -56,38 +66,44 @@ __device__ __forceinline__ float log2_split(float x) {
 template <typename CodeT>
 __global__ void __launch_bounds__(256)
 logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n_bits,
-                     const uint2* __restrict__ x, CodeT* __restrict__ codes,
+                     const uint4* __restrict__ x, CodeT* __restrict__ codes,
                      float* __restrict__ lmin_out, float* __restrict__ step_out) {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, grp = lane / kLanesPerTile, sub = lane % kLanesPerTile;
     const int kmax = (1 << (n_bits - 1)) - 1;
     const uint32_t sign_bit = 1u << (n_bits - 1);
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-    // kTilesInFlight tiles per warp and step: their loads are issued together
-    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesInFlight;
-         t0 < n_tiles; t0 += nwarps * kTilesInFlight) {
-      uint2 raws[kTilesInFlight];
+    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesPerWarpStep;
+         t0 < n_tiles; t0 += nwarps * kTilesPerWarpStep) {
+      uint4 raws[kTilesPerLane][2];
 #pragma unroll
-      for (int j = 0; j < kTilesInFlight; ++j) {
-        const int64_t t = t0 + j < n_tiles ? t0 + j : t0;
-        raws[j] = x[((t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4) / 4];
+      for (int j = 0; j < kTilesPerLane; ++j) {  // every load of the step first
+        int64_t t = t0 + j * (32 / kLanesPerTile) + grp;
+        t = t < n_tiles ? t : t0;
+        const int64_t e0 = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + sub * 16;  // element
+        raws[j][0] = x[e0 / 8];
+        raws[j][1] = x[e0 / 8 + 1];
       }
 #pragma unroll
-      for (int j = 0; j < kTilesInFlight; ++j) {
-        const int64_t t = t0 + j;
-        if (t >= n_tiles) break;
-        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
-        const uint2 raw = raws[j];
-        float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
+      for (int j = 0; j < kTilesPerLane; ++j) {
+        const int64_t t = t0 + j * (32 / kLanesPerTile) + grp;
+        const int64_t e0 = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + sub * 16;
+        const uint32_t w[8] = {raws[j][0].x, raws[j][0].y, raws[j][0].z, raws[j][0].w,
+                               raws[j][1].x, raws[j][1].y, raws[j][1].z, raws[j][1].w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
         float amax = 0.f, amin = INFINITY;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 16; ++i) {
             const float a = fabsf(v[i]);
             amax = fmaxf(amax, a);
             if (a > 0.f) amin = fminf(amin, a);
         }
-        amax = warp_max(amax);
-        amin = warp_min(amin);
+        amax = group_max(amax);
+        amin = group_min(amin);
         float step2 = 0.f, l2min = 0.f;
         if (amax > 0.f) {
             const float l2max = log2_split(amax);
@@ -95,7 +111,7 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             l2min = l2max - span2;
             step2 = __fdividef(span2, static_cast<float>(kmax - 1));
         }
-        uint32_t c[4];
+        uint32_t c[16];
         if (step2 > 0.f) {
             const float inv = __fdividef(1.f, step2);
             const float theta = log2_split(0.5f + 0.5f * ex2_approx(step2)) * inv;  // linear midpoint, in steps
@@ -106,7 +122,7 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             const bool tiny = l2min < -100.f;
             const float anchor = tiny ? 1.f : ex2_approx(-l2min);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 const float a = fabsf(v[i]);
                 int K = 0;
                 if (a > 0.f) {
@@ -123,17 +139,26 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             }
         } else {  // all zero (K = 0), or one magnitude (K = 1)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 16; ++i)
                 c[i] = (fabsf(v[i]) > 0.f ? 1u : 0u) | (signbit(v[i]) ? sign_bit : 0u);
         }
-        if (sizeof(CodeT) == 1) {
-            *reinterpret_cast<uint32_t*>(codes + base) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-        } else {
-            *reinterpret_cast<uint2*>(codes + base) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-        }
-        if (lane == 0) {
-            lmin_out[t] = l2min * kLn2;
-            step_out[t] = step2 * kLn2;
+        if (t < n_tiles) {
+            if (sizeof(CodeT) == 1) {
+                uint32_t q[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[k] = c[4 * k] | (c[4 * k + 1] << 8) | (c[4 * k + 2] << 16) | (c[4 * k + 3] << 24);
+                *reinterpret_cast<uint4*>(codes + e0) = make_uint4(q[0], q[1], q[2], q[3]);
+            } else {
+                uint32_t q[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) q[k] = c[2 * k] | (c[2 * k + 1] << 16);
+                *reinterpret_cast<uint4*>(codes + e0) = make_uint4(q[0], q[1], q[2], q[3]);
+                *reinterpret_cast<uint4*>(codes + e0 + 8) = make_uint4(q[4], q[5], q[6], q[7]);
+            }
+            if (sub == 0) {
+                lmin_out[t] = l2min * kLn2;
+                step_out[t] = step2 * kLn2;
+            }
         }
       }
     }
@@ -143,64 +168,69 @@ template <typename CodeT>
 __global__ void __launch_bounds__(256)
 logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n_bits,
                      const CodeT* __restrict__ codes, const float* __restrict__ lmin,
-                     const float* __restrict__ step, uint2* __restrict__ y) {
-    const int lane = threadIdx.x & 31;
+                     const float* __restrict__ step, uint4* __restrict__ y) {
+    const int lane = threadIdx.x & 31, grp = lane / kLanesPerTile, sub = lane % kLanesPerTile;
     const uint32_t kmask = (1u << (n_bits - 1)) - 1u;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesInFlight;
-         t0 < n_tiles; t0 += nwarps * kTilesInFlight) {
-      uint2 raws[kTilesInFlight];
-      float lms[kTilesInFlight], sts[kTilesInFlight];
+    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kTilesPerWarpStep;
+         t0 < n_tiles; t0 += nwarps * kTilesPerWarpStep) {
+      uint4 raws[kTilesPerLane][2];
+      float lms[kTilesPerLane], sts[kTilesPerLane];
 #pragma unroll
-      for (int j = 0; j < kTilesInFlight; ++j) {  // every load of the step in flight together
-        const int64_t t = t0 + j < n_tiles ? t0 + j : t0;
-        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
-        if (sizeof(CodeT) == 1) raws[j] = make_uint2(*reinterpret_cast<const uint32_t*>(codes + base), 0u);
-        else raws[j] = *reinterpret_cast<const uint2*>(codes + base);
+      for (int j = 0; j < kTilesPerLane; ++j) {  // every load of the step in flight together
+        int64_t t = t0 + j * (32 / kLanesPerTile) + grp;
+        t = t < n_tiles ? t : t0;
+        const int64_t e0 = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + sub * 16;
+        raws[j][0] = *reinterpret_cast<const uint4*>(codes + e0);
+        raws[j][1] = sizeof(CodeT) == 1 ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(codes + e0 + 8);
         lms[j] = lmin[t];
         sts[j] = step[t];
       }
 #pragma unroll
-      for (int j = 0; j < kTilesInFlight; ++j) {
-        const int64_t t = t0 + j;
-        if (t >= n_tiles) break;
-        const int64_t base = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + lane * 4;
-        uint32_t c[4];
+      for (int j = 0; j < kTilesPerLane; ++j) {
+        const int64_t t = t0 + j * (32 / kLanesPerTile) + grp;
+        if (t >= n_tiles) continue;
+        const int64_t e0 = (t / tiles_per_row) * cols + (t % tiles_per_row) * 128 + sub * 16;
+        uint32_t c[16];
         if (sizeof(CodeT) == 1) {
-            const uint32_t w = raws[j].x;
+            const uint32_t w[4] = {raws[j][0].x, raws[j][0].y, raws[j][0].z, raws[j][0].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c[i] = (w >> (8 * i)) & 0xffu;
+            for (int i = 0; i < 16; ++i) c[i] = (w[i / 4] >> (8 * (i % 4))) & 0xffu;
         } else {
-            const uint2 w = raws[j];
-            c[0] = w.x & 0xffffu; c[1] = w.x >> 16; c[2] = w.y & 0xffffu; c[3] = w.y >> 16;
+            const uint32_t w[8] = {raws[j][0].x, raws[j][0].y, raws[j][0].z, raws[j][0].w,
+                                   raws[j][1].x, raws[j][1].y, raws[j][1].z, raws[j][1].w};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) c[i] = (w[i / 2] >> (16 * (i % 2))) & 0xffffu;
         }
         // g1 = e^min once per tile; Step2 = Step * log2(e) as an exact pair (hi + lo)
         const float st = sts[j];
         const float g1 = expf(lms[j]);
         const float s_hi = st * kLog2e;
         const float s_lo = fmaf(st, kLog2e, -s_hi) + st * kLog2eLo;
-        uint16_t o[4];
+        uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 16; ++i) {
             const uint32_t K = c[i] & kmask;
             float m = 0.f;
             if (K) {
                 const float k = static_cast<float>(K - 1);
                 const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
                 const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
-                const float ip = floorf(e_hi);
+                const float ip = floorf(e_hi);  // 0 .. 32 for metadata the encoder wrote
                 const float f = ex2_approx(e_hi - ip) * fmaf(e_lo, kLn2, 1.f);
-                m = ldexpf(g1 * f, static_cast<int>(ip));
+                m = ip < 127.f ? (g1 * f) * exp2_int(static_cast<int>(ip)) : ldexpf(g1 * f, static_cast<int>(ip));
             }
-            o[i] = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
+            const uint32_t b = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
+            o[i / 2] = (i % 2) ? (o[i / 2] | (b << 16)) : b;
         }
-        y[base / 4] = make_uint2(o[0] | (static_cast<uint32_t>(o[1]) << 16), o[2] | (static_cast<uint32_t>(o[3]) << 16));
+        y[e0 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+        y[e0 / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
 }
 
 unsigned warp_grid(int64_t n_tiles) {
-    const int64_t blocks = ceil_div(n_tiles, 8 * kTilesInFlight);
+    const int64_t blocks = ceil_div(n_tiles, 8 * kTilesPerWarpStep);
     return static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16);
 }
 
@@ -218,10 +248,10 @@ extern "C" moe_status moe_logfmt_encode(int32_t n_bits, int64_t rows, int64_t co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (n_bits <= 8)
         logfmt_encode_kernel<uint8_t><<<warp_grid(n_tiles), 256, 0, s>>>(
-            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint2*>(x), static_cast<uint8_t*>(codes), lmin, step);
+            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint4*>(x), static_cast<uint8_t*>(codes), lmin, step);
     else
         logfmt_encode_kernel<uint16_t><<<warp_grid(n_tiles), 256, 0, s>>>(
-            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint2*>(x), static_cast<uint16_t*>(codes), lmin, step);
+            n_tiles, tpr, cols, n_bits, reinterpret_cast<const uint4*>(x), static_cast<uint16_t*>(codes), lmin, step);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
@@ -236,10 +266,10 @@ extern "C" moe_status moe_logfmt_decode(int32_t n_bits, int64_t rows, int64_t co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (n_bits <= 8)
         logfmt_decode_kernel<uint8_t><<<warp_grid(n_tiles), 256, 0, s>>>(
-            n_tiles, tpr, cols, n_bits, static_cast<const uint8_t*>(codes), lmin, step, reinterpret_cast<uint2*>(y));
+            n_tiles, tpr, cols, n_bits, static_cast<const uint8_t*>(codes), lmin, step, reinterpret_cast<uint4*>(y));
     else
         logfmt_decode_kernel<uint16_t><<<warp_grid(n_tiles), 256, 0, s>>>(
-            n_tiles, tpr, cols, n_bits, static_cast<const uint16_t*>(codes), lmin, step, reinterpret_cast<uint2*>(y));
+            n_tiles, tpr, cols, n_bits, static_cast<const uint16_t*>(codes), lmin, step, reinterpret_cast<uint4*>(y));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -48,6 +48,7 @@ _SIGS = {
     "moe_config_validate": [_cfgp],
     "moe_workspace_size": [_cfgp, _i64, ctypes.POINTER(_sz)],
     "moe_gate": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "moe_gate_quant": [_cfgp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_quant_1x128": [_i64, _i64, _vp, _vp, _vp, _vp],
     "moe_quant_128x128": [_i64, _i64, _i64, _vp, _vp, _vp, _vp],
     "moe_quant_1x128_pow2": [_i64, _i64, _vp, _vp, _vp, _vp],
@@ -170,6 +171,15 @@ def moe_gate(cfg, x, Wg, bias, topk_idx, topk_w, counts, stream=None):
     T = x.shape[0]
     _check("moe_gate", _lib_handle().moe_gate(ctypes.byref(_cfg(cfg)), T, _ptr(x), _ptr(Wg), _ptr(bias),
                                               _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _stream(stream)))
+
+
+def moe_gate_quant(cfg, x, Wg, bias, topk_idx, topk_w, counts, xq, xs, stream=None):
+    """moe_gate plus the 1x128 quantisation of x (xq [T, H] codes, xs [T, H/128] scales) in one
+    pass over x; raises MoEError with status MOE_ERR_UNSUPPORTED outside the fused kernel."""
+    T = x.shape[0]
+    _check("moe_gate_quant", _lib_handle().moe_gate_quant(
+        ctypes.byref(_cfg(cfg)), T, _ptr(x), _ptr(Wg), _ptr(bias), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(xq), _ptr(xs), _stream(stream)))
 
 
 def moe_quant_1x128(x, q, s, stream=None):

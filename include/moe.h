@@ -131,6 +131,19 @@ MOE_API moe_status moe_gate(const moe_config* cfg, int64_t T, const void* x, con
                     const float* bias, int32_t* topk_idx, float* topk_w, int32_t* counts,
                     moe_stream_t stream);
 
+/* a1 + a2 fused ([P1] §2.2 MoEGate; [P2] §3.2 1x128 activation tiles; no counterpart on the
+ * pages as one call): moe_gate, plus the 1x128 FP8 quantisation of the same x as moe_quant_1x128
+ * (MOE_FP8_BLOCK) or moe_quant_1x128_pow2 (MOE_MXFP8) writes it, bit for bit, while x
+ * streams through the gate once.
+ *  xq [T, H] E4M3 codes, 16-byte aligned; xs [T, H/128] FP32 scales.
+ *  Returns MOE_ERR_UNSUPPORTED (and launches nothing) for configurations outside the fused
+ *  kernel: FP32 mode, E not a multiple of 32 or above 256, E / n_group not a multiple of 32,
+ *  n_group > 8, top_k > 8, H % 128 != 0, or x / Wg / xq not 16-byte aligned; callers then
+ *  use moe_gate and moe_quant_1x128. */
+MOE_API moe_status moe_gate_quant(const moe_config* cfg, int64_t T, const void* x, const void* Wg,
+                                  const float* bias, int32_t* topk_idx, float* topk_w,
+                                  int32_t* counts, uint8_t* xq, float* xs, moe_stream_t stream);
+
 /* a2. [P2] §3.2 activation quantisation in 1x128 tiles.  For every row and every 128
  * consecutive columns: amax = max |x|; scale = amax / 448 and q = E4M3(x * (448 / amax))
  * (round to nearest even, saturating to +-448); amax == 0 gives scale 1 and q = 0.

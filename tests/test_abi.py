@@ -202,6 +202,27 @@ def test_more_host_side_rejections(moe):
     assert L.moe_device_error(None) == INV
 
 
+def test_gate_quant_host_side_rejections(moe):
+    # refused (INVALID_ARG) or declined (UNSUPPORTED) before any CUDA call, so no GPU is needed
+    L = moe._lib_handle()
+    vp = ctypes.c_void_p
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    INV, UNS = moe.MOE_ERR_INVALID_ARG, moe.MOE_ERR_UNSUPPORTED
+    cfg = lambda **kw: ctypes.byref(moe.make_config(dict(sy.config("v3_prefill"), **kw)))  # noqa: E731
+    ok_args = (vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None)
+    assert L.moe_gate_quant(cfg(), -1, *ok_args) == INV
+    assert L.moe_gate_quant(cfg(), 8, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None, vp(16), None) == INV
+    assert L.moe_gate_quant(cfg(), 8, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None, None) == INV
+    assert L.moe_gate_quant(cfg(n_group=7), 8, *ok_args) == INV
+    # shapes outside the fused kernel: FP32 mode, groups of 16 experts, 288 experts
+    assert L.moe_gate_quant(ctypes.byref(moe.make_config(sy.config("tiny_fp32"))), 8, *ok_args) == UNS
+    assert L.moe_gate_quant(cfg(n_group=16, topk_group=4), 8, *ok_args) == UNS
+    assert L.moe_gate_quant(cfg(n_experts=288, n_group=9, topk_group=2), 8, *ok_args) == UNS
+    # misaligned x or codes
+    assert L.moe_gate_quant(cfg(), 8, vp(24), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None) == UNS
+    assert L.moe_gate_quant(cfg(), 8, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(24), vp(16), None) == UNS
+
+
 def test_logfmt_host_side_rejections(moe):
     L = moe._lib_handle()
     vp = ctypes.c_void_p

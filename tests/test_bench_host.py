@@ -23,8 +23,10 @@ def test_stage_work_matches_the_layer_closed_forms():
     # the gate reads x (BF16) and Wg once; the combine reads 9 BF16 rows and writes y per token
     assert w["gate"][1] >= T * H * 2 and w["gate"][1] < T * H * 2 * 1.05
     assert w["combine"][1] >= (K + 1) * T * H * 2 + T * H * 2
-    for k in ("gate", "quant", "permute", "combine"):
+    for k in ("gate", "quant", "gate_quant", "permute", "combine"):
         assert w[k][0] == "hbm"
+    # fused, x is read once: the two stages' bytes less one read of x
+    assert w["gate_quant"][1] == w["gate"][1] + w["quant"][1] - T * H * 2
     # no shared expert: one row per routed slot only
     cfg0 = dict(cfg, has_shared=0)
     assert bench.stage_work(cfg0)["gemm2_down"][1] == T * K * 2 * I * H
