@@ -10,12 +10,13 @@
 // the grid points floor(r) + 1 and floor(r) + 2, and the linear midpoint of two neighbours is
 // at the fraction theta = log2((1 + 2^Step2) / 2) / Step2 of the way between them in log
 // space (the same for every pair of the tile), so K = floor(r) + 1 + (frac(r) >= theta);
-// below g1 the midpoint with zero is at r = -1 / Step2.  Logarithms are taken as the
-// exponent plus log2 of the significand in [1, 2) (hardware approximation, absolute error
-// near 2^-22), so r is within about 1e-4 of a step for n <= 12 (the step shrinks as
-// 2^-(n-1)).  Decoding forms 2^(Step2 (K - 1)) from an exactly split exponent (integer part,
-// fraction, and the FMA residual of the product), times g1 = e^min computed once per tile,
-// a few 1e-7 off the exact value before its rounding to BF16.
+// below g1 the midpoint with zero is at r = -1 / Step2.  Logarithms are the hardware base-2
+// approximation (absolute error near 2^-22; per tile, for the min and max, as the exponent
+// plus the log2 of the significand so that subnormal magnitudes are covered), so r is within
+// about 1e-4 of a step for n <= 12 (the step shrinks as 2^-(n-1)).  Decoding forms
+// 2^(Step2 (K - 1)) from the hardware exponential of the rounded product and the FMA residual
+// of the product, times g1 = e^min computed once per tile, a few 1e-7 off the exact value
+// before its rounding to BF16.
 // Eight lanes per tile, 16 values per lane (two 16-byte BF16 loads), so the tile's reductions
 // take three shuffle steps and its per-tile arithmetic is shared by 16 values; each lane takes
 // kTilesPerLane tiles per step with every load issued first.  2 bytes read and 1 (n <= 8) or
@@ -47,6 +48,12 @@ __device__ __forceinline__ float group_min(float v) {
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -126,13 +133,13 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
                 const float a = fabsf(v[i]);
                 int K = 0;
                 if (a > 0.f) {
-                    const float r = (tiny ? log2_split(a) - l2min : log2_split(a * anchor)) * inv;  // 0 at g1
+                    // 0 at g1; a * anchor is a normal number (the hardware logarithm, absolute
+                    // error near 2^-22, far below the decision margins)
+                    const float r = (tiny ? log2_split(a) - l2min : lg2_approx(a * anchor)) * inv;
                     if (r < 0.f) {
                         K = r >= zero_cut ? 1 : 0;
-                    } else {
-                        const float fl = floorf(r);
-                        K = static_cast<int>(fl) + 1 + (r - fl >= theta ? 1 : 0);
-                        K = K > kmax ? kmax : K;
+                    } else {  // floor(r) + 1, plus 1 from the fraction theta on: floor(r - theta) + 2
+                        K = min(__float2int_rd(r - theta) + 2, kmax);
                     }
                 }
                 c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
@@ -216,9 +223,9 @@ logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
                 const float k = static_cast<float>(K - 1);
                 const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
                 const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
-                const float ip = floorf(e_hi);  // 0 .. 32 for metadata the encoder wrote
-                const float f = ex2_approx(e_hi - ip) * fmaf(e_lo, kLn2, 1.f);
-                m = ip < 127.f ? (g1 * f) * exp2_int(static_cast<int>(ip)) : ldexpf(g1 * f, static_cast<int>(ip));
+                // 2^e_hi by the hardware exponential (exact range reduction, relative error near
+                // 2^-22), e_hi in 0 .. 32 for metadata the encoder wrote
+                m = g1 * (ex2_approx(e_hi) * fmaf(e_lo, kLn2, 1.f));
             }
             const uint32_t b = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
             o[i / 2] = (i % 2) ? (o[i / 2] | (b << 16)) : b;
