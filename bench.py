@@ -72,7 +72,7 @@ def parse():
     p.add_argument("--groups", type=int, default=None)
     p.add_argument("--topk-group", type=int, default=None)
     # one stage alone (a profiler's target with a small device footprint)
-    p.add_argument("--only", choices=["gate"], default=None)
+    p.add_argument("--only", choices=["gate", "gate_quant"], default=None)
     return p.parse_args()
 
 
@@ -576,7 +576,8 @@ def run_reference(args, cfg, rank, world):
 
 
 def run_only(args, cfg):
-    """moe_gate alone on the workload's tokens: K timed calls after W warm-up calls."""
+    """moe_gate (or moe_gate_quant) alone on the workload's tokens: K timed calls after W warm-up
+    calls."""
     torch.cuda.set_device(0)
     T = cfg["T"]
     inp = sy.make_inputs(cfg, "cuda", weights=False)
@@ -585,6 +586,11 @@ def run_only(args, cfg):
     x = inp["x"].view(torch.uint16) if fp8 else inp["x"]
     Wg = inp["Wg"].view(torch.uint16) if fp8 else inp["Wg"]
     call = lambda: moe.moe_gate(cfg, x, Wg, inp["bias"], out["topk_idx"], out["topk_w"], out["counts"])  # noqa: E731
+    if args.only == "gate_quant":
+        xq = torch.empty(T, cfg["hidden"], dtype=torch.uint8, device="cuda")
+        xs = torch.empty(T, cfg["hidden"] // 128, dtype=torch.float32, device="cuda")
+        call = lambda: moe.moe_gate_quant(cfg, x, Wg, inp["bias"], out["topk_idx"], out["topk_w"],  # noqa: E731
+                                          out["counts"], xq, xs)
     for _ in range(max(args.warmup, 3)):
         call()
     torch.cuda.synchronize()
@@ -595,8 +601,8 @@ def run_only(args, cfg):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    nbytes = stage_work(cfg)["gate"][1]
-    print(json.dumps({"stage": "gate", "workload": cfg["name"], "T": T, "us_per_call": ms * 1e3,
+    nbytes = stage_work(cfg)[args.only][1]
+    print(json.dumps({"stage": args.only, "workload": cfg["name"], "T": T, "us_per_call": ms * 1e3,
                       "GB/s": nbytes / ms / 1e6, "steps": args.steps}), flush=True)
 
 

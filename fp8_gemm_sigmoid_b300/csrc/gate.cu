@@ -13,9 +13,9 @@
 //    (each reads half of the token's groups from TMEM, the pair exchanges group scores and
 //    merges two local top-k lists through shared memory).  The kernel streams x once.
 //    With xq / xs given it also quantises x into 1x128 FP8 tiles (précis §3.2) while the
-//    tiles pass through shared memory for the MMA: four otherwise idle warps read each
-//    128-column block of their token row from the operand ring, so x is read from HBM once
-//    for the gate and the quantisation together.
+//    tiles pass through shared memory for the MMA: eight otherwise idle warps, two threads
+//    per token row, read each 128-column block from the operand ring, so x is read from HBM
+//    once for the gate and the quantisation together.
 //  - gate_fused_kernel (FP32 inputs, or shapes outside the tensor-core kernel's range): the
 //    [kTok, E] logit tile is formed in shared memory on the CUDA cores, then each warp runs
 //    the selection for its tokens with warp shuffles (lane l holds experts l, l+32, ...).
@@ -231,10 +231,12 @@ constexpr int kGtBBytes = kGtMaxE * kGtK * 2;    // 32 KB (E rows)
 constexpr int kGtStageBytes = kGtABytes + kGtBBytes;
 constexpr int kGqStageBytes = 32 * 128;    // one quantising warp's 32 rows x 128 codes
 constexpr int kGqOff = kGtStages * kGtStageBytes + 4096;  // 1024-aligned: the TMA store swizzle
-constexpr int kGtSmem = kGqOff + 4 * kGqStageBytes + 1024;
+constexpr int kGqRedOff = kGqOff + 4 * kGqStageBytes;    // [2][128] partial amax of the two halves
+constexpr int kGtSmem = kGqRedOff + 2 * 128 * 4 + 1024;
 constexpr long long kGtWaitBudget = 4000000000LL;
-constexpr int kGqWarp0 = 4;         // warps 4..7 quantise x (one token row per thread)
-constexpr int kGqWarps = 4;
+constexpr int kGqWarp0 = 4;         // warps 4..11 quantise x: two threads per token row, one per
+constexpr int kGqWarps = 8;         // 64-column half of each 128-column block
+constexpr int kGqBar = 1;           // their named barrier
 
 __device__ int g_gate_error = 0;
 
@@ -265,53 +267,17 @@ __device__ __forceinline__ uint2 code8(uint4 c, float mul, int e) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// Quantises one 1x128 tile of a token row, exactly as quant_1x128_kernel does, from its two
-// 64-column halves in the operand ring (rows of 128 bytes, 16-byte chunk j at chunk position
-// j ^ r7, the 128-byte swizzle): its 128 codes to the 128-byte row `out` (16-byte chunk j at
-// chunk position j ^ r7 again) and its scale to *sc.
-__device__ __forceinline__ void quant_row_block(const uint8_t* half0, const uint8_t* half1, int r7, int pow2,
-                                                uint8_t* out, float* sc) {
-    const uint8_t* hp[2] = {half0, half1};
-    float amax = 0.f;
+// max |v| over one thread's 64 BF16 values (8 chunks of 8), four independent chains
+__device__ __forceinline__ float amax64(const uint4 (&c)[8]) {
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint4 c = *reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4));
-            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
-        }
-    if (amax == 0.f) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(out + ((j ^ r7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-        *sc = 1.f;
-        return;
+        for (int k = 0; k < 4; ++k)
+            m[k] = fmaxf(m[k], fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
     }
-    if (pow2) {
-        const int e = pow2_exponent(amax);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const uint2 a = code8<true>(*reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4)), 0.f, e);
-                const uint2 b = code8<true>(*reinterpret_cast<const uint4*>(hp[h] + (((j + 1) ^ r7) << 4)), 0.f, e);
-                *reinterpret_cast<uint4*>(out + (((h * 4 + j / 2) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
-            }
-        *sc = exp2_int(e);
-    } else {
-        const float mul = __fdiv_rn(448.f, amax);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const uint2 a = code8<false>(*reinterpret_cast<const uint4*>(hp[h] + ((j ^ r7) << 4)), mul, 0);
-                const uint2 b = code8<false>(*reinterpret_cast<const uint4*>(hp[h] + (((j + 1) ^ r7) << 4)), mul, 0);
-                *reinterpret_cast<uint4*>(out + (((h * 4 + j / 2) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
-            }
-        *sc = __fdiv_rn(amax, 448.f);
-    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
 // sigmoid with the fast exponential and division intrinsics (a few ulp in FP32; the selection
@@ -348,7 +314,8 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGtStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + (quant ? kGqWarps : 0));  // the MMA commit (+ the quantisers)
+            // the MMA commit, and the four quantising warps of the half the stage holds
+            mbar_init(&empty[s], 1 + (quant ? kGqWarps / 2 : 0));
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
@@ -423,40 +390,69 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             mma_commit(acc_full);  // fires when every MMA above has completed
         }
     } else if (quant && warp >= kGqWarp0 && warp < kGqWarp0 + kGqWarps) {
-        // 1x128 quantisation of x from the operand ring: thread r owns token row r of the
-        // tile.  Even stages hold the first half of a 128-column block and odd stages the
-        // second; once both have landed the block is coded from shared memory and both
-        // stages are released (the ring holds four).
-        // The codes go out through a per-warp staging box [32 rows][128 B] (the same 128-byte
-        // swizzle) by TMA stores, which clip the rows past T; the scales are stored directly.
-        const int r = (warp - kGqWarp0) * 32 + lane;
+        // 1x128 quantisation of x from the operand ring.  Even stages hold the first 64 columns
+        // of a 128-column block and odd stages the rest; thread (half, r) owns half `half` of
+        // token row r of the tile.  Per block: each thread loads its 64 values from its stage
+        // (128-byte swizzle: 16-byte chunk j of row r at chunk position j ^ (r % 8)) and
+        // releases the stage, the two halves exchange their amax, and each codes its half
+        // exactly as quant_1x128_kernel does into a per-row-quarter staging box [32 rows][128 B]
+        // (the same swizzle) that one lane sends out by a TMA store, which clips the rows past
+        // T; the scales are stored directly.
+        const int half = (warp - kGqWarp0) / 4, quarter = warp & 3;
+        const int r = quarter * 32 + lane, r7 = r & 7;
         const int64_t t = t0 + r;
         const int nb = p.H / 128;
-        uint8_t* stg = smem + kGqOff + (warp - kGqWarp0) * kGqStageBytes;
+        uint8_t* stg = smem + kGqOff + quarter * kGqStageBytes + lane * 128;
+        float* red = reinterpret_cast<float*>(smem + kGqRedOff);  // [2][128]
+        const bool issuer = half == 0 && lane == 0;
         bool ok = true;
-        for (int it = 0; it + 1 < nk; it += 2) {  // stage it % kGtStages, phase parity (it / kGtStages) & 1
-            const int s = it % kGtStages, s1 = (it + 1) % kGtStages;
-            const uint32_t ph = (it / kGtStages) & 1u, ph1 = ((it + 1) / kGtStages) & 1u;
-            if (!mbar_wait(&full[s], ph, abort_flag, kGtWaitBudget) ||
-                !mbar_wait(&full[s1], ph1, abort_flag, kGtWaitBudget)) { ok = false; break; }
-            const int kb = ((it + kc0) % nk) / 2;
-            if (lane == 0) sched::tma_store_wait_read();  // the previous box has left the staging
+        for (int it = half; it < nk; it += 2) {  // this thread's stage: it % kGtStages, parity (it / kGtStages) & 1
+            const int s = it % kGtStages;
+            const uint32_t ph = (it / kGtStages) & 1u;
+            ok = ok && mbar_wait(&full[s], ph, abort_flag, kGtWaitBudget);
+            uint4 c[8];
+            const uint8_t* row = smem + s * kGtStageBytes + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4*>(row + ((j ^ r7) << 4));
+            red[half * 128 + r] = amax64(c);
             __syncwarp();
-            float sc;
-            quant_row_block(smem + s * kGtStageBytes + r * 128, smem + s1 * kGtStageBytes + r * 128, r & 7,
-                            p.pow2, stg + lane * 128, &sc);
-            __syncwarp();
-            if (lane == 0) {  // this warp is done with both stages
-                mbar_arrive(&empty[s]);
-                mbar_arrive(&empty[s1]);
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+            if (issuer) sched::tma_store_wait_read();  // the previous box has left the staging
+            named_bar_sync(kGqBar, kGqWarps * 32);     // both halves' amax; the staging is free
+            const float amax = fmaxf(red[r], red[128 + r]);
+            const int kb = ((it - half + kc0) % nk) / 2;
+            if (amax == 0.f) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(stg + (((half * 4 + j) ^ r7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            } else if (p.pow2) {
+                const int e = pow2_exponent(amax);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint2 a = code8<true>(c[2 * j], 0.f, e), b = code8<true>(c[2 * j + 1], 0.f, e);
+                    *reinterpret_cast<uint4*>(stg + (((half * 4 + j) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+                }
+            } else {
+                const float mul = __fdiv_rn(448.f, amax);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint2 a = code8<false>(c[2 * j], mul, 0), b = code8<false>(c[2 * j + 1], mul, 0);
+                    *reinterpret_cast<uint4*>(stg + (((half * 4 + j) ^ r7) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+                }
             }
             sched::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                sched::tma_store_2d(&tmQ, stg, kb * 128, static_cast<int32_t>(t0 + (warp - kGqWarp0) * 32));
-            if (t < p.T) p.xs[t * nb + kb] = sc;
+            named_bar_sync(kGqBar, kGqWarps * 32);     // the box's rows are complete
+            if (half == 0) {
+                if (lane == 0)
+                    sched::tma_store_2d(&tmQ, smem + kGqOff + quarter * kGqStageBytes, kb * 128,
+                                        static_cast<int32_t>(t0 + quarter * 32));
+                if (t < p.T) {
+                    const int e = pow2_exponent(amax);
+                    p.xs[t * nb + kb] = amax == 0.f ? 1.f : (p.pow2 ? exp2_int(e) : __fdiv_rn(amax, 448.f));
+                }
+            }
         }
-        if (lane == 0) sched::tma_store_wait_all();  // every code has reached global memory
+        if (issuer) sched::tma_store_wait_all();  // every code has reached global memory
         if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicCAS(&g_gate_error, 0, 0x204);
