@@ -410,16 +410,18 @@ class OracleLayer:
     quantised on the oracle side beforehand: quantisation of the weights is an offline step on
     both sides, so no timed region contains it."""
 
-    def __init__(self, cfg, layer):
+    def __init__(self, cfg, inp):
+        """inp: the workload's inputs as synthetic.make_inputs draws them (BF16 expert weights
+        included)."""
         import numpy as np
         import oracle
         self.np, self.oracle, self.cfg = np, oracle, cfg
         self.pow2 = cfg["mode"] == "mxfp8"
         self.ocfg = dict(cfg, mode="fp8_pow2") if self.pow2 else cfg  # the oracle's name of the mode
-        self.x = layer.inp["x"].view(torch.uint16).cpu().numpy()
-        self.Wg = layer.inp["Wg"].view(torch.uint16).cpu().numpy()
-        self.bias = layer.inp["bias"].cpu().numpy()
-        self.W13, self.W2 = layer.inp["W13"], layer.inp["W2"]
+        self.x = inp["x"].view(torch.uint16).cpu().numpy()
+        self.Wg = inp["Wg"].view(torch.uint16).cpu().numpy()
+        self.bias = inp["bias"].cpu().numpy()
+        self.W13, self.W2 = inp["W13"], inp["W2"]
         self.cache = {}
 
     def qweights(self, ids):
@@ -466,7 +468,7 @@ def cpu_baseline(cfg, layer, n_sample):
     output row depends only on its own token, so the expert part extrapolates per token:
     tokens/s = T / (gate time + expert time * T / n_sample)."""
     T = cfg["T"]
-    ol = OracleLayer(cfg, layer)
+    ol = OracleLayer(cfg, layer.inp)
     sample = sy.sample_tokens(T, n_sample, seed=2).numpy()
     g = ol.gate(slice(0, T))
     ol.prepare(g, sample)  # weights quantised outside the timed passes
@@ -487,9 +489,11 @@ def run_reference(args, cfg, rank, world):
     if rank != 0:
         return
     import numpy as np
-    torch.cuda.set_device(0)
-    layer = Layer(cfg, "cuda:0")
-    ol = OracleLayer(cfg, layer)
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    if dev != "cpu":
+        torch.cuda.set_device(0)
+    # the workload's inputs, drawn as for the library's arm; nothing of the library runs here
+    ol = OracleLayer(cfg, sy.make_inputs(cfg, dev))
     T = cfg["T"]
     n_gate = min(args.ref_gate_tokens, T)
     n_exp = min(args.ref_sample, n_gate)
@@ -544,35 +548,6 @@ def config_dict(cfg, world):
             "n_experts": cfg["n_experts"], "top_k": cfg["top_k"], "shared": cfg["has_shared"],
             "l2": "inputs larger than L2 (11.3 GB of FP8 expert weights per step)",
             "parallelism": "replicas x%d" % world}
-
-
-def run_reference(args, cfg, rank, world):
-    """The reference arm: the CPU oracle timed on the host cores, rank 0 only."""
-    if rank != 0:
-        return
-    torch.cuda.set_device(0)
-    layer = Layer(cfg, "cuda:0")
-    n = max(1, min(args.cpu_sample // 4, cfg["T"]))
-    for _ in range(args.warmup):
-        cpu_baseline(cfg, layer, n)
-    times = []
-    threads = 1
-    for _ in range(args.steps):
-        dt, threads = cpu_baseline(cfg, layer, n)
-        times.append(dt)
-    tot = sum(times)
-    val = n * args.steps / tot
-    line = {
-        "impl": "reference", "metric": metric_name(cfg), "value": val,
-        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(cfg, 1),
-        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": "first %d tokens of the %s batch as a layer of their own, per step" % (n, cfg["name"])},
-        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
 
 
 def run_only(args, cfg):

@@ -128,3 +128,18 @@ def test_gemm_bytes_count_the_hit_experts_once():
     pb = bench.gemm_bytes(prefill, np.ones(prefill["n_experts"]))
     assert pb["gemm1_swiglu"] / (peaks["hbm"] * 1e9) < bench.stage_work(prefill)["gemm1_swiglu"][1] / (
         2 * peaks["bf16"] * 1e12)
+
+
+def test_reference_arm_runs_the_oracle_plan(capsys):
+    # the reference arm on a small FP8 layer, on the CPU: one JSON line describing the plan
+    import json
+    import types
+    cfg = sy.config("v3_decode", T=96, hidden=256, inter=128, n_experts=16, n_group=4, topk_group=2, top_k=4)
+    args = types.SimpleNamespace(ref_gate_tokens=64, ref_sample=16, steps=2, warmup=1)
+    bench.run_reference(args, cfg, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and "16-token sample" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    bench.run_reference(args, cfg, 1, 2)          # other ranks print nothing
+    assert capsys.readouterr().out == ""
