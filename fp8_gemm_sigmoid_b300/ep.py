@@ -81,14 +81,15 @@ def exchange_rows(send, send_counts, recv_counts, group=None):
 
 class EPLayer:
     """The MoE layer forward with the routed experts split over the ranks of `group` (one GPU
-    each).  weights: this rank's FP8 expert weights, its E / N routed experts followed by the
+    each), in either FP8 mode.  weights: this rank's FP8 expert weights, its E / N routed experts followed by the
     shared expert (W13 [E/N + 1, 2I, H], W13_s, W2 [E/N + 1, H, I], W2_s, as moe_quant_128x128
     writes them) and the whole gate weight Wg [E, H] (BF16)."""
 
     def __init__(self, cfg, weights, group=None, device="cuda"):
         self.cfg = dict(cfg)
-        if self.cfg["mode"] != "fp8" or not self.cfg["has_shared"]:
-            raise ValueError("the EP layer runs the FP8 mode with a shared expert")
+        if self.cfg["mode"] not in ("fp8", "mxfp8") or not self.cfg["has_shared"]:
+            raise ValueError("the EP layer runs an FP8 mode with a shared expert")
+        self.mx = self.cfg["mode"] == "mxfp8"  # power-of-two scales (weights from pow2=True)
         self.group = group
         self.world = dist.get_world_size(group) if dist.is_initialized() else 1
         self.rank = dist.get_rank(group) if dist.is_initialized() else 0
@@ -106,6 +107,16 @@ class EPLayer:
     def _slice(self, name, lo, hi):
         return self.w[name][lo:hi]
 
+    def _down(self, n_groups, offs, rows, hq, hs, lo, hi, out):
+        """The down-projection GEMM of experts [lo, hi) into BF16 rows."""
+        c = self.cfg
+        if self.mx:
+            moe.moe_grouped_gemm_mxfp8(n_groups, offs, rows, c["hidden"], c["inter"], hq, hs, self._slice("W2", lo, hi),
+                                       self._slice("W2_s", lo, hi), moe.MOE_EPI_STORE, out, None)
+        else:
+            moe.moe_grouped_gemm_fp8(n_groups, offs, rows, c["hidden"], c["inter"], hq, hs, self._slice("W2", lo, hi),
+                                     self._slice("W2_s", lo, hi), moe.MOE_EPI_STORE, out, None, None)
+
     def forward(self, x, bias, y, topk_idx, topk_w, counts):
         c, H, I, K = self.cfg, self.cfg["hidden"], self.cfg["inter"], self.cfg["top_k"]
         T = x.shape[0]
@@ -115,7 +126,7 @@ class EPLayer:
         moe.moe_gate(c, x, self.w["Wg"], bias, topk_idx, topk_w, counts)
         xq = torch.empty(T, H, dtype=u8, device=dev)
         xs = torch.empty(T, H // 128, dtype=f32, device=dev)
-        moe.moe_quant_1x128(x, xq, xs)
+        (moe.moe_quant_1x128_pow2 if self.mx else moe.moe_quant_1x128)(x, xq, xs)
         R = T * K
         offs = torch.empty(self.E + 1, dtype=i32, device=dev)
         perm_tok = torch.empty(R, dtype=i32, device=dev)
@@ -152,10 +163,9 @@ class EPLayer:
             hs = torch.empty(I // 128, n, dtype=f32, device=dev)
             moe.moe_grouped_gemm_fp8_gather(self.ep, offs_l, n, 2 * I, H, perm_l, recv_q, recv_s,
                                             self._slice("W13", lo, hi), self._slice("W13_s", lo, hi),
-                                            moe.MOE_EPI_SWIGLU_QUANT, hq, hs)
+                                            moe.MOE_EPI_SWIGLU_QUANT, hq, hs, mx=self.mx)
             yl = torch.empty(n, H, dtype=torch.bfloat16, device=dev)
-            moe.moe_grouped_gemm_fp8(self.ep, offs_l, n, H, I, hq, hs, self._slice("W2", lo, hi),
-                                     self._slice("W2_s", lo, hi), moe.MOE_EPI_STORE, yl, None, None)
+            self._down(self.ep, offs_l, n, hq, hs, lo, hi, yl)
             # 5. back to receive order: a one-slot combine with weight 1 is an exact row gather
             ones = torch.ones(n, 1, dtype=f32, device=dev)
             moe.moe_combine(self.cfg_local, n, yl, row_l, ones, None, y_recv)
@@ -169,8 +179,8 @@ class EPLayer:
         ysh = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
         sh = self.ep
         moe.moe_grouped_gemm_fp8_gather(1, offs_s, T, 2 * I, H, ident, xq, xs, self._slice("W13", sh, sh + 1),
-                                        self._slice("W13_s", sh, sh + 1), moe.MOE_EPI_SWIGLU_QUANT, hq_s, hs_s)
-        moe.moe_grouped_gemm_fp8(1, offs_s, T, H, I, hq_s, hs_s, self._slice("W2", sh, sh + 1),
-                                 self._slice("W2_s", sh, sh + 1), moe.MOE_EPI_STORE, ysh, None, None)
+                                        self._slice("W13_s", sh, sh + 1), moe.MOE_EPI_SWIGLU_QUANT, hq_s, hs_s,
+                                        mx=self.mx)
+        self._down(1, offs_s, T, hq_s, hs_s, sh, sh + 1, ysh)
         moe.moe_combine(c, T, y_routed, row_of, topk_w, ysh, y)
         return dict(send=s_splits, recv=r_splits)

@@ -29,15 +29,16 @@ def one_rank_group():
         dist.destroy_process_group()
 
 
+@pytest.mark.parametrize("mode", ["fp8", "mxfp8"])
 @pytest.mark.parametrize("E,G,TG,K,T", [(64, 2, 1, 4, 300), (16, 4, 2, 2, 129)])
-def test_ep_layer_one_rank_equals_moe_forward(one_rank_group, E, G, TG, K, T):
+def test_ep_layer_one_rank_equals_moe_forward(one_rank_group, E, G, TG, K, T, mode):
     from fp8_gemm_sigmoid_b300 import build, ep, moe, synthetic as sy
     build.build()
     torch.cuda.set_device(0)
     cfg = sy.config("v3_decode", T=T, hidden=512, inter=256, n_experts=E, n_group=G, topk_group=TG,
-                    top_k=K, seed=21)
+                    top_k=K, seed=21, mode=mode)
     inp = sy.make_inputs(cfg, DEV)
-    q = moe.quantize_weights(inp["W13"], inp["W2"])
+    q = moe.quantize_weights(inp["W13"], inp["W2"], pow2=mode == "mxfp8")
     x = inp["x"].view(torch.uint16)
     Wg = inp["Wg"].view(torch.uint16)
     ref = moe.empty_outputs(cfg, T)
