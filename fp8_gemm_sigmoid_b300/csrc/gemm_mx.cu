@@ -376,32 +376,35 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 // valid rows directly, so that no write reaches the next group's rows
                 const bool half1 = b_block(p, c, 1) < p.N / 128;
                 const bool full_warp = c.row0 + q * 32 + 32 <= c.row_end;
-                if (lane == 0) tma_store_wait_read();  // the staging boxes are free again
-                __syncwarp();
+                // All four 64-column boxes are read from TMEM and converted to BF16 pairs first,
+                // so that the accumulator goes back to the MMA before any store is made.
+                uint32_t pk[4][32];
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx) {
                     float v[64];
                     tmem_ld32(taddr + bx * 64, *reinterpret_cast<float(*)[32]>(&v[0]));
                     tmem_ld32(taddr + bx * 64 + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
                     tmem_ld_wait_regs(*reinterpret_cast<float(*)[32]>(&v[0]), *reinterpret_cast<float(*)[32]>(&v[32]));
-                    if (bx == 3) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-                    if (bx >= 2 && !half1) continue;
-                    uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                        pk[bx][i] = *reinterpret_cast<const uint32_t*>(&b2);
                     }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) tma_store_wait_read();  // the staging boxes are free again
+                __syncwarp();
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx) {
+                    if (bx >= 2 && !half1) continue;
                     if (full_warp) {
                         uint8_t* box = my_stage + bx * kOutBox;
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             *reinterpret_cast<uint4*>(box + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                make_uint4(pk[bx][4 * j], pk[bx][4 * j + 1], pk[bx][4 * j + 2], pk[bx][4 * j + 3]);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) tma_store_2d(&tmO, box, c.n_tile * kBN + bx * 64, c.row0 + q * 32);
@@ -409,7 +412,8 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                                               static_cast<int64_t>(row) * p.N + c.n_tile * kBN + bx * 64);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_uint4(pk[bx][4 * j], pk[bx][4 * j + 1], pk[bx][4 * j + 2], pk[bx][4 * j + 3]);
                     }
                 }
             }

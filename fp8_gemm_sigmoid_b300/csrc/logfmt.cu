@@ -123,26 +123,34 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             const float inv = __fdividef(1.f, step2);
             const float theta = log2_split(0.5f + 0.5f * ex2_approx(step2)) * inv;  // linear midpoint, in steps
             const float zero_cut = -inv;
-            // 1 / g1, unless g1 lies so low (tiles of subnormal BF16 values) that 1 / g1 would
-            // overflow; then the logarithm is taken first and g1's subtracted (a rare, slower
-            // and slightly less precise path)
             const bool tiny = l2min < -100.f;
-            const float anchor = tiny ? 1.f : ex2_approx(-l2min);
+            if (!tiny) {
+                // u = r - theta with r = log2(a / g1) / Step2, 0 at g1: a * anchor is a normal
+                // number (the hardware logarithm, absolute error near 2^-22, far below the
+                // decision margins); a = 0 gives u = -inf and K = 0.  For r >= 0 the code is
+                // floor(r) + 1, plus 1 from the fraction theta on: floor(u) + 2.
+                const float anchor = ex2_approx(-l2min);
+                const float cut1 = zero_cut - theta;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float a = fabsf(v[i]);
-                int K = 0;
-                if (a > 0.f) {
-                    // 0 at g1; a * anchor is a normal number (the hardware logarithm, absolute
-                    // error near 2^-22, far below the decision margins)
-                    const float r = (tiny ? log2_split(a) - l2min : lg2_approx(a * anchor)) * inv;
-                    if (r < 0.f) {
-                        K = r >= zero_cut ? 1 : 0;
-                    } else {  // floor(r) + 1, plus 1 from the fraction theta on: floor(r - theta) + 2
-                        K = min(__float2int_rd(r - theta) + 2, kmax);
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    const float u = fmaf(lg2_approx(fabsf(v[i]) * anchor), inv, -theta);
+                    const int K = u >= -theta ? min(__float2int_rd(u) + 2, kmax) : (u >= cut1 ? 1 : 0);
+                    c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
                 }
-                c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
+            } else {
+                // g1 so low (tiles of subnormal BF16 values) that 1 / g1 would overflow: the
+                // logarithm is taken first and g1's subtracted (a rare, slower and slightly less
+                // precise path)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = fabsf(v[i]);
+                    int K = 0;
+                    if (a > 0.f) {
+                        const float r = (log2_split(a) - l2min) * inv;
+                        K = r < 0.f ? (r >= zero_cut ? 1 : 0) : min(__float2int_rd(r - theta) + 2, kmax);
+                    }
+                    c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
+                }
             }
         } else {  // all zero (K = 0), or one magnitude (K = 1)
 #pragma unroll
@@ -214,21 +222,23 @@ logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
         const float g1 = expf(lms[j]);
         const float s_hi = st * kLog2e;
         const float s_lo = fmaf(st, kLog2e, -s_hi) + st * kLog2eLo;
-        uint32_t o[8];
+        float m[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t K = c[i] & kmask;
-            float m = 0.f;
-            if (K) {
-                const float k = static_cast<float>(K - 1);
-                const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
-                const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
-                // 2^e_hi by the hardware exponential (exact range reduction, relative error near
-                // 2^-22), e_hi in 0 .. 32 for metadata the encoder wrote
-                m = g1 * (ex2_approx(e_hi) * fmaf(e_lo, kLn2, 1.f));
-            }
-            const uint32_t b = f32_to_bf16_bits((c[i] >> (n_bits - 1)) ? -m : m);
-            o[i / 2] = (i % 2) ? (o[i / 2] | (b << 16)) : b;
+            const float k = static_cast<float>(static_cast<int>(K) - 1);
+            const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
+            const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
+            // 2^e_hi by the hardware exponential (exact range reduction, relative error near
+            // 2^-22), e_hi in 0 .. 32 for metadata the encoder wrote
+            const float mag = K ? g1 * (ex2_approx(e_hi) * fmaf(e_lo, kLn2, 1.f)) : 0.f;
+            m[i] = (c[i] >> (n_bits - 1)) ? -mag : mag;
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // paired round-to-nearest-even BF16 conversion
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(m[2 * i], m[2 * i + 1]);
+            o[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
         y[e0 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
         y[e0 / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
