@@ -782,7 +782,7 @@ def main():
                 "frac_of_burst": amount / dom_t / 1e12 / (peaks["bf16"] * FP8_PER_BF16)}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": amount / dom_t / 1e9, "peak": peaks["hbm"],
-                "unit": "GB/s", "peak_source": "%s copy bandwidth" % peaks["src"]}
+                "unit": "GB/s", "peak_source": "%s copy bandwidth, of %s" % (peaks["src"], peaks["src"])}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"], roof["traffic_source"] = measured_traffic(dom, cfg)
     roof["algorithmic"] = amount
