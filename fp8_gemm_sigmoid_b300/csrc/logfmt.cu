@@ -112,9 +112,12 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
         amax = group_max(amax);
         amin = group_min(amin);
         float step2 = 0.f, l2min = 0.f;
+        bool held = false;  // min raised to max - ln 2^32: values below g1 exist
         if (amax > 0.f) {
             const float l2max = log2_split(amax);
-            const float span2 = fminf(l2max - log2_split(amin), 32.f);  // max - min held <= log2 2^32
+            const float full_span = l2max - log2_split(amin);
+            held = full_span > 32.f;
+            const float span2 = fminf(full_span, 32.f);  // max - min held <= log2 2^32
             l2min = l2max - span2;
             step2 = __fdividef(span2, static_cast<float>(kmax - 1));
         }
@@ -129,13 +132,25 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
                 // number (the hardware logarithm, absolute error near 2^-22, far below the
                 // decision margins); a = 0 gives u = -inf and K = 0.  For r >= 0 the code is
                 // floor(r) + 1, plus 1 from the fraction theta on: floor(u) + 2.
+                // Unless the min was held, every non-zero value lies at or above g1 (u at least
+                // -theta, up to the logarithm's error, so floor(u) + 2 >= 1), and zeros give
+                // u = -inf: K = floor(u) + 2 clamped to [0, kmax] covers every value.
                 const float anchor = ex2_approx(-l2min);
-                const float cut1 = zero_cut - theta;
+                if (!held) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float u = fmaf(lg2_approx(fabsf(v[i]) * anchor), inv, -theta);
-                    const int K = u >= -theta ? min(__float2int_rd(u) + 2, kmax) : (u >= cut1 ? 1 : 0);
-                    c[i] = static_cast<uint32_t>(K) | (signbit(v[i]) ? sign_bit : 0u);
+                    for (int i = 0; i < 16; ++i) {
+                        const float u = fmaf(lg2_approx(fabsf(v[i]) * anchor), inv, -theta);
+                        const int K = min(max(__float2int_rd(u) + 2, 0), kmax);
+                        c[i] = static_cast<uint32_t>(K) | ((__float_as_uint(v[i]) >> (32 - n_bits)) & sign_bit);
+                    }
+                } else {  // values below g1: K = 1 down to the linear midpoint with zero, else 0
+                    const float cut1 = zero_cut - theta;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float u = fmaf(lg2_approx(fabsf(v[i]) * anchor), inv, -theta);
+                        const int K = u >= -theta ? min(__float2int_rd(u) + 2, kmax) : (u >= cut1 ? 1 : 0);
+                        c[i] = static_cast<uint32_t>(K) | ((__float_as_uint(v[i]) >> (32 - n_bits)) & sign_bit);
+                    }
                 }
             } else {
                 // g1 so low (tiles of subnormal BF16 values) that 1 / g1 would overflow: the
@@ -161,12 +176,14 @@ logfmt_encode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
             if (sizeof(CodeT) == 1) {
                 uint32_t q[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = c[4 * k] | (c[4 * k + 1] << 8) | (c[4 * k + 2] << 16) | (c[4 * k + 3] << 24);
+                for (int k = 0; k < 4; ++k)  // bytes c0 c1 c2 c3
+                    q[k] = __byte_perm(__byte_perm(c[4 * k], c[4 * k + 1], 0x0040),
+                                       __byte_perm(c[4 * k + 2], c[4 * k + 3], 0x0040), 0x5410);
                 *reinterpret_cast<uint4*>(codes + e0) = make_uint4(q[0], q[1], q[2], q[3]);
             } else {
                 uint32_t q[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) q[k] = c[2 * k] | (c[2 * k + 1] << 16);
+                for (int k = 0; k < 8; ++k) q[k] = __byte_perm(c[2 * k], c[2 * k + 1], 0x5410);
                 *reinterpret_cast<uint4*>(codes + e0) = make_uint4(q[0], q[1], q[2], q[3]);
                 *reinterpret_cast<uint4*>(codes + e0 + 8) = make_uint4(q[4], q[5], q[6], q[7]);
             }
@@ -225,14 +242,15 @@ logfmt_decode_kernel(int64_t n_tiles, int64_t tiles_per_row, int64_t cols, int n
         float m[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const uint32_t K = c[i] & kmask;
-            const float k = static_cast<float>(static_cast<int>(K) - 1);
+            const float fK = static_cast<float>(c[i] & kmask);
+            const float k = fK - 1.f;
             const float e_hi = s_hi * k;                        // 2^(Step2 k) = 2^e_hi * 2^e_lo
-            const float e_lo = fmaf(s_hi, k, -e_hi) + s_lo * k;
+            const float e_lo = fmaf(s_lo, k, fmaf(s_hi, k, -e_hi));
             // 2^e_hi by the hardware exponential (exact range reduction, relative error near
-            // 2^-22), e_hi in 0 .. 32 for metadata the encoder wrote
-            const float mag = K ? g1 * (ex2_approx(e_hi) * fmaf(e_lo, kLn2, 1.f)) : 0.f;
-            m[i] = (c[i] >> (n_bits - 1)) ? -mag : mag;
+            // 2^-22), e_hi in 0 .. 32 for metadata the encoder wrote; K = 0 gives 0 through the
+            // factor min(K, 1), the sign bit is moved into place
+            const float mag = g1 * (ex2_approx(e_hi) * fmaf(e_lo, kLn2, 1.f)) * fminf(fK, 1.f);
+            m[i] = __uint_as_float(__float_as_uint(mag) | ((c[i] << (32 - n_bits)) & 0x80000000u));
         }
         uint32_t o[8];
 #pragma unroll
