@@ -197,17 +197,19 @@ class Layer:
         self.hq = torch.empty(R, I, dtype=u8, device=dev)
         self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)  # K-block-major
         self.yexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
-        # FP8 modes: the gate quantises x in the same pass when its tensor-core kernel takes the
-        # shape (moe_forward then launches no separate quantiser); the staged pass does the same
+        # FP8 modes: from MOE_GATE_QUANT_MIN_TOKENS tokens up the gate quantises x in the same
+        # pass when its tensor-core kernel takes the shape (moe_forward then launches no separate
+        # quantiser); the staged pass does the same
         self.fused = False
-        try:
-            o = self.out
-            moe.moe_gate_quant(cfg, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"], o["counts"],
-                               self.xq, self.xs)
-            self.fused = True
-        except moe.MoEError as e:
-            if e.status != moe.MOE_ERR_UNSUPPORTED:
-                raise
+        if cfg["T"] >= moe.MOE_GATE_QUANT_MIN_TOKENS:
+            try:
+                o = self.out
+                moe.moe_gate_quant(cfg, self.x, self.weights["Wg"], self.bias, o["topk_idx"], o["topk_w"],
+                                   o["counts"], self.xq, self.xs)
+                self.fused = True
+            except moe.MoEError as e:
+                if e.status != moe.MOE_ERR_UNSUPPORTED:
+                    raise
         self.stages = (["gate_quant"] if self.fused else ["gate", "quant"]) + Layer.STAGES[2:]
 
     def forward(self, world=1):

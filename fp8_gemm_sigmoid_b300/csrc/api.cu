@@ -225,11 +225,12 @@ extern "C" moe_status moe_forward(const moe_config* cfg, int64_t T, const void* 
     void* gscratch = base + L.gemm_scratch;
     const size_t gbytes = L.total - L.gemm_scratch;
 
-    // FP8 modes: the gate also writes the 1x128 quantisation of x when its tensor-core kernel
-    // takes the shape (x is then read once); otherwise the quantiser runs on its own below
+    // FP8 modes: from MOE_GATE_QUANT_MIN_TOKENS tokens up the gate also writes the 1x128
+    // quantisation of x when its tensor-core kernel takes the shape (x is then read once);
+    // otherwise the quantiser runs on its own below
     uint8_t* xq = fp8 ? reinterpret_cast<uint8_t*>(base + L.xq) : nullptr;
     float* xs = fp8 ? reinterpret_cast<float*>(base + L.xs) : nullptr;
-    const bool fused = fp8 && gate_quant_supported(c) && aligned16(w->Wg);
+    const bool fused = fp8 && T >= MOE_GATE_QUANT_MIN_TOKENS && gate_quant_supported(c) && aligned16(w->Wg);
     if (fused) MOE_TRY(moe_gate_quant(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, xq, xs, stream));
     else MOE_TRY(moe_gate(cfg, T, x, w->Wg, bias, topk_idx, topk_w, counts, stream));
     if (update_bias) MOE_TRY(moe_bias_update(cfg, T, counts, bias, stream));

@@ -19,6 +19,7 @@ CHECKS_LIB_PATH = os.path.join(_HERE, "libmoe_checks.so")  # the -DMOE_CHECKS de
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
 MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8 = 0, 1, 2
 MOE_EPI_SWIGLU_QUANT, MOE_EPI_STORE = 0, 1
+MOE_GATE_QUANT_MIN_TOKENS = 6144  # moe_forward fuses the quantisation into the gate from here up
 
 
 class MoEError(RuntimeError):

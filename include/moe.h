@@ -144,6 +144,12 @@ MOE_API moe_status moe_gate_quant(const moe_config* cfg, int64_t T, const void* 
                                   const float* bias, int32_t* topk_idx, float* topk_w,
                                   int32_t* counts, uint8_t* xq, float* xs, moe_stream_t stream);
 
+/* moe_forward takes moe_gate_quant from this many tokens up.  The fused kernel's pace is set
+ * by its quantising warps, about 100 us per 128-token CTA on a B300 whatever T, so for fewer
+ * tokens moe_gate and moe_quant_1x128 launched apart finish first (69 against 103 us at
+ * T = 256; 113 against 98 us at T = 8192). */
+#define MOE_GATE_QUANT_MIN_TOKENS 6144
+
 /* a2. [P2] §3.2 activation quantisation in 1x128 tiles.  For every row and every 128
  * consecutive columns: amax = max |x|; scale = amax / 448 and q = E4M3(x * (448 / amax))
  * (round to nearest even, saturating to +-448); amax == 0 gives scale 1 and q = 0.
@@ -307,7 +313,8 @@ MOE_API moe_status moe_bias_update(const moe_config* cfg, int64_t T, const int32
 /* The whole layer forward ([P1] §2.2 MoEGate and the layer's routed + shared experts;
  * [P1] §2.3 dispatch and combine, done on one GPU as a permutation and a gather; [P2] §3.1
  * 8 routed + 1 shared expert per token; [P2] §3.2 the fine-grained FP8 expert GEMMs) on one
- * stream: gate (a1), quantisation (a2, FP8 mode),
+ * stream: gate (a1), quantisation (a2, FP8 mode; in the gate's pass from
+ * MOE_GATE_QUANT_MIN_TOKENS tokens up where moe_gate_quant takes the shape),
  * permutation (a3), grouped GEMM with SwiGLU (a4), grouped GEMM down-projection (a5), with
  * the shared expert as the last group (a6), combine (a7) and, if update_bias != 0, the bias
  * update (a8) after routing.

@@ -152,6 +152,19 @@ def test_binding_signatures_match_the_header():
         assert c == py, (name, c, py)
 
 
+def test_binding_constants_match_the_header():
+    # the status codes, modes, epilogues and the fused-gate threshold the binding mirrors
+    from fp8_gemm_sigmoid_b300 import moe as m
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    values = {k: int(v) for k, v in re.findall(r"\b(MOE_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    values.update({k: int(v) for k, v in re.findall(r"#define\s+(MOE_[A-Z0-9_]+)\s+(\d+)", src)})
+    names = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA",
+             "MOE_ERR_TIMEOUT", "MOE_FP32", "MOE_FP8_BLOCK", "MOE_MXFP8", "MOE_EPI_SWIGLU_QUANT", "MOE_EPI_STORE",
+             "MOE_GATE_QUANT_MIN_TOKENS"]
+    for n in names:
+        assert values[n] == getattr(m, n), n
+
+
 def test_more_host_side_rejections(moe):
     # every case below is refused before any CUDA call, so it runs without a GPU
     L = moe._lib_handle()

@@ -47,7 +47,8 @@ def test_bench_line_has_the_contract_keys():
     assert e["d2h_bytes_per_step"] >= 2048 * 7168 * 2            # y, BF16, plus the routing
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1 and "16-token sample" in c["sample"]
-    assert d["gpu_launches"] == 9 * 3 or d["gpu_launches"] == 10 * 3   # fused gate: 9 per step
+    # below MOE_GATE_QUANT_MIN_TOKENS the gate and the quantiser run apart: 10 launches per step
+    assert d["gpu_launches"] == 10 * 3
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
 
 

@@ -1,8 +1,9 @@
 """moe_gate_quant (the gate with the 1x128 quantisation of x fused in), called through the C ABI:
 its routing, weights and counts must be moe_gate's and its codes and scales moe_quant_1x128's
 (moe_quant_1x128_pow2's in MXFP8 mode), bit for bit, on ragged token counts over several
-tiles, with all-zero and saturating tiles.  moe_forward takes this path in both FP8 modes,
-so the layer parity tests against the oracle cover it as well."""
+tiles, with all-zero and saturating tiles.  moe_forward takes this path in both FP8 modes from
+MOE_GATE_QUANT_MIN_TOKENS tokens up, so the full-size layer parity tests against the oracle
+(8192 tokens and more) cover it as well, and the smaller layers cover the two kernels apart."""
 import numpy as np
 import pytest
 import torch
