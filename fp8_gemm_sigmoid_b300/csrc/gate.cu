@@ -267,17 +267,30 @@ __device__ __forceinline__ uint2 code8(uint4 c, float mul, int e) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// max |v| over one thread's 64 BF16 values (8 chunks of 8), four independent chains
+// Lane-wise maximum of two pairs of BF16 values (a NaN lane yields the other operand's lane,
+// as fmaxf does).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// max |v| over one thread's 64 BF16 values (8 chunks of 8), four independent chains.  The
+// maximum is taken on the packed values with their sign bits cleared (a maximum of BF16 values
+// is one of them, so it equals the FP32 maximum of the widened values), two values per
+// instruction, and only the last pair is widened.
 __device__ __forceinline__ float amax64(const uint4 (&c)[8]) {
-    float m[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr uint32_t kAbs = 0x7fff7fffu;
+    uint32_t m[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            m[k] = fmaxf(m[k], fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+        m[0] = bf16x2_max(m[0], c[j].x & kAbs);
+        m[1] = bf16x2_max(m[1], c[j].y & kAbs);
+        m[2] = bf16x2_max(m[2], c[j].z & kAbs);
+        m[3] = bf16x2_max(m[3], c[j].w & kAbs);
     }
-    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    const uint32_t v = bf16x2_max(bf16x2_max(m[0], m[1]), bf16x2_max(m[2], m[3]));
+    return fmaxf(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 // sigmoid with the fast exponential and division intrinsics (a few ulp in FP32; the selection
@@ -406,6 +419,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         float* red = reinterpret_cast<float*>(smem + kGqRedOff);  // [2][128]
         const bool issuer = half == 0 && lane == 0;
         bool ok = true;
+        int kb = kc0 / 2;                        // the 128-column block of this iteration (kc0 is even)
         for (int it = half; it < nk; it += 2) {  // this thread's stage: it % kGtStages, parity (it / kGtStages) & 1
             const int s = it % kGtStages;
             const uint32_t ph = (it / kGtStages) & 1u;
@@ -420,7 +434,6 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if (issuer) sched::tma_store_wait_read();  // the previous box has left the staging
             named_bar_sync(kGqBar, kGqWarps * 32);     // both halves' amax; the staging is free
             const float amax = fmaxf(red[r], red[128 + r]);
-            const int kb = ((it - half + kc0) % nk) / 2;
             if (amax == 0.f) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -451,6 +464,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     p.xs[t * nb + kb] = amax == 0.f ? 1.f : (p.pow2 ? exp2_int(e) : __fdiv_rn(amax, 448.f));
                 }
             }
+            if (++kb == nb) kb = 0;
         }
         if (issuer) sched::tma_store_wait_all();  // every code has reached global memory
         if (!ok && lane == 0) {
