@@ -29,6 +29,10 @@ def _inputs(T, H, E, seed):
         x[1] = 0                       # every tile of the row is zero: scale 1, codes 0
         x[2, :128] *= 1e4              # large values beside small ones
         x[3, 128:256] = -3.0           # one magnitude
+    if T > 4:
+        # a tile of BF16 subnormals (below 2^-126), both signs: the fused kernel's packed
+        # maximum must see them as the quantiser's FP32 maximum does
+        x[4, 256:384] = torch.linspace(-3e-39, 5e-39, 128, device=DEV)
     x = x.to(torch.bfloat16)
     Wg = (torch.randn(E, H, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
     bias = (torch.rand(E, generator=g, device=DEV) - 0.5) * 0.1
