@@ -46,7 +46,8 @@ using namespace sm100;
 using namespace sched;
 
 constexpr int kBK = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 3;     // operand ring; over sparse groups a 4th stage takes the place of
+constexpr int kMaxStages = 4;  // the down GEMM's output staging (every row is then stored directly)
 constexpr int kABytes = kBM * kBK;          // 16 KB
 constexpr int kBBytes = kBN * kBK;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -63,13 +64,14 @@ constexpr int kScaleSlots = 16;  // K blocks of scale copies in flight (covers L
 constexpr int kSlotFloats = 132;  // 128 activation scales, 2 weight scales, padding to 16 bytes
 // Control block after the operand ring and the output staging (byte offsets): barriers,
 // TMEM address and flags, amax exchange, warp sums, scale ring, then the tile prefix.
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 2 * kScaleSlots;  // full/empty, pfull/pempty,
+constexpr int kNumBars = 2 * kMaxStages + 2 + 2 + 1 + 1 + 2 * kScaleSlots;  // full/empty, pfull/pempty,
                                                                       // mma_done, ebar, sfull/sempty
 constexpr int kCtlBars = 0, kCtlSlot = (kNumBars * 8 + 15) / 16 * 16, kCtlRed = kCtlSlot + 16,
               kCtlWarpSums = kCtlRed + 2048,
               kCtlScales = kCtlWarpSums + 64, kCtlTiles = kCtlScales + kScaleSlots * kSlotFloats * 4;
 constexpr int kSmemFixed = 1024 + kStages * kStageBytes + kOutBytes + kCtlTiles;
 constexpr int kSmemMax = kSmemFixed + 4 * (kMaxGroups + 1);
+static_assert((kMaxStages - kStages) * kStageBytes <= kOutBytes, "the 4th stage lives in the output staging");
 
 enum : int { kErrTimeoutProducer = 0x101, kErrTimeoutMma = 0x102, kErrTimeoutEpilogue = 0x103,
              kErrTimeoutScales = 0x104 };
@@ -108,6 +110,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // boundary, where the FP32 accumulation order already decides.  g -> -inf gives -0.
 __device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// kRing: operand ring stages, kStages or kMaxStages.  With kMaxStages the last stage occupies
+// the output staging, so the down GEMM's epilogue stores every row directly.
+template <int kRing>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -118,15 +123,16 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint8_t* out_stage = smem + kStages * kStageBytes;   // [8 warps][2 halves][32 x 128 B]
     uint8_t* ctl = out_stage + kOutBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ctl + kCtlBars);
-    uint64_t* full = bars;                  // [kStages]  TMA -> MMA
-    uint64_t* empty = bars + kStages;       // [kStages]  MMA -> TMA
-    uint64_t* pfull = bars + 2 * kStages;   // [2]        MMA -> epilogue
+    static_assert(kRing == kStages || kRing == kMaxStages, "ring depth");
+    uint64_t* full = bars;                  // [kRing]    TMA -> MMA
+    uint64_t* empty = bars + kMaxStages;    // [kRing]    MMA -> TMA
+    uint64_t* pfull = bars + 2 * kMaxStages;  // [2]      MMA -> epilogue
     uint64_t* pempty = pfull + 2;           // [2]        epilogue -> MMA
     uint64_t* mma_done = pempty + 2;        // [1]        final MMA drain
     uint64_t* ebar = mma_done + 1;          // [1]        epilogue amax exchange (one phase per tile)
     uint64_t* sfull = ebar + 1;             // [kScaleSlots] scale loaders -> epilogue
     uint64_t* sempty = sfull + kScaleSlots; // [kScaleSlots] epilogue -> scale loaders
-    static_assert(2 * kStages + 6 + 2 * kScaleSlots <= kNumBars, "barrier block");
+    static_assert(2 * kMaxStages + 6 + 2 * kScaleSlots <= kNumBars, "barrier block");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + kCtlSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;   // stays 0: drains wait for in-flight work, not for aborts
@@ -137,7 +143,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRing; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -204,7 +210,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         tma_load_2d(sb + kBBytes / 2, &tmB, &full[s], kb * kBK, brow1);
                     }
                     ++issued;
-                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                    if (++s == kRing) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok && lane == 0) {
@@ -213,8 +219,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             // let every issued copy land before the CTA can exit
             if (lane == 0) {
-                for (int i = 0; i < kStages && i < issued; ++i) {
-                    if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+                for (int i = 0; i < kRing && i < issued; ++i) {
+                    if (--s < 0) { s = kRing - 1; ph ^= 1u; }
                     mbar_wait(&full[s], ph, never, kWaitBudget);
                 }
             }
@@ -242,7 +248,7 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     mma_commit(&pfull[b]);
                     pbits ^= 1u << b;
                     b ^= 1;
-                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                    if (++s == kRing) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
@@ -411,8 +417,8 @@ grouped_gemm_fp8_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 // and one lane writes each 32 x 64 box with a TMA store; a warp holding the
                 // group's ragged end stores its valid rows directly, so that no write reaches
                 // the next group's rows.
-                const bool full_warp = c.row0 + quarter * 32 + 32 <= c.row_end;
-                if (lane == 0) tma_store_wait_read();  // the staging boxes are free again
+                const bool full_warp = kRing == kStages && c.row0 + quarter * 32 + 32 <= c.row_end;
+                if (lane == 0 && kRing == kStages) tma_store_wait_read();  // the staging boxes are free again
                 __syncwarp();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -542,12 +548,23 @@ moe_status launch_grouped_gemm_fp8_tc(int32_t n_groups, const int32_t* offs, int
     p.out_s = out_s;
     static PerDeviceOnce attr_once;
     MOE_CUDA_CHECK(once_per_device(attr_once, [] {
-        return cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel<kStages>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(grouped_gemm_fp8_tc_kernel<kMaxStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemMax);
+        return e;
     }));
     const int64_t max_tiles = (ceil_div(rows, kBM) + n_groups) * p.n_tiles_n;
     const int grid = static_cast<int>(max_tiles < device_sm_count() ? max_tiles : device_sm_count());
     const int smem = kSmemFixed + 4 * (n_groups + 1);
-    grouped_gemm_fp8_tc_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, tmO, p);
+    // Sparse groups (fewer than 64 rows each on average, as in decoding) leave the tensor cores
+    // idle and make the weight stream from HBM the bound: the kernel then takes a 4th operand
+    // stage to keep more of it in flight (few of its warps would fill a 32-row staging box
+    // anyway).  Over full groups the 3-stage ring is faster.
+    const bool deep = rows < 64LL * n_groups;
+    if (deep) grouped_gemm_fp8_tc_kernel<kMaxStages><<<grid, kThreads, smem, s>>>(tmA, tmB, tmO, p);
+    else grouped_gemm_fp8_tc_kernel<kStages><<<grid, kThreads, smem, s>>>(tmA, tmB, tmO, p);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -247,7 +247,10 @@ def _random_groups(rng, E, total, empty=()):
     return c
 
 
-@pytest.mark.parametrize("H,I,E,R", [(384, 256, 5, 700), (640, 384, 3, 400), (7168, 2048, 4, 300)])
+# (1024, 256, 24, 400): fewer than 64 rows per group on average, the 4-stage ring with every
+# output row stored directly (some groups still hold more than 32 rows)
+@pytest.mark.parametrize("H,I,E,R", [(384, 256, 5, 700), (640, 384, 3, 400), (7168, 2048, 4, 300),
+                                     (1024, 256, 24, 400)])
 def test_grouped_gemm_fp8_swiglu_and_down(moe, orc, H, I, E, R):
     rng = np.random.default_rng(H + R)
     counts = _random_groups(rng, E, R, empty=(1,))
