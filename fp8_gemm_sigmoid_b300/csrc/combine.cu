@@ -71,6 +71,70 @@ combine_bf16_kernel(int64_t T, int H, int K, const uint16_t* __restrict__ yexp,
     }
 }
 
+// The same for 4 <= K <= 8, with every load of a token's slots issued before any of them is
+// used: the slots' row indices and weights first, then up to eight 16-byte row loads and the
+// shared expert's, so that a thread keeps nine row loads in flight instead of one.  The sums run
+// in slot order with the same operations, so the result is the general kernel's bit for bit.
+// (For K = 1 or 2 the general kernel's higher occupancy wins: measured on the top-1 layer.)
+__global__ void __launch_bounds__(256)
+combine_bf16_k8_kernel(int64_t T, int H, int K, const uint16_t* __restrict__ yexp,
+                       const int32_t* __restrict__ row_of, const float* __restrict__ w,
+                       const uint16_t* __restrict__ yshared, uint16_t* __restrict__ y) {
+    constexpr int kMaxK = 8;
+    const int chunks = H / 8;
+    const int64_t total = T * chunks;
+    const int64_t rows = T * K;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / chunks;
+        const int ch = static_cast<int>(i % chunks);
+        int64_t r[kMaxK];
+        float wk[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            r[k] = k < K ? row_of[t * K + k] : -1;
+            wk[k] = k < K ? w[t * K + k] : 0.f;
+        }
+        uint4 v[kMaxK];
+        bool use[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            use[k] = k < K && r[k] >= 0 && r[k] < rows;
+            (void)MOE_DCHECK(g_combine_check, k >= K || use[k] || r[k] == -1, 0x302);
+            v[k] = use[k] ? *reinterpret_cast<const uint4*>(yexp + r[k] * H + ch * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const uint4 vs = yshared ? *reinterpret_cast<const uint4*>(yshared + t * H + ch * 8) : make_uint4(0u, 0u, 0u, 0u);
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (!use[k]) continue;  // a dropped slot adds nothing
+            const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wk[k], __uint_as_float(u[j] << 16)));
+                acc[2 * j + 1] =
+                    __fadd_rn(acc[2 * j + 1], __fmul_rn(wk[k], __uint_as_float(u[j] & 0xffff0000u)));
+            }
+        }
+        if (yshared) {
+            const uint32_t u[4] = {vs.x, vs.y, vs.z, vs.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(u[j] << 16));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(u[j] & 0xffff0000u));
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j])) |
+                   (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j + 1])) << 16);
+        *reinterpret_cast<uint4*>(y + t * H + ch * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // FP32 rows: one thread per (token, 4 columns).
 __global__ void __launch_bounds__(256)
 combine_f32_kernel(int64_t T, int H, int K, const float* __restrict__ yexp,
@@ -140,6 +204,10 @@ extern "C" moe_status moe_combine(const moe_config* cfg, int64_t T, const void* 
         combine_f32_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, static_cast<const float*>(yexp),
                                                 row_of, topk_w, static_cast<const float*>(yshared),
                                                 static_cast<float*>(y));
+    else if (c.top_k >= 4 && c.top_k <= 8)
+        combine_bf16_k8_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, static_cast<const uint16_t*>(yexp),
+                                                    row_of, topk_w, static_cast<const uint16_t*>(yshared),
+                                                    static_cast<uint16_t*>(y));
     else
         combine_bf16_kernel<<<grid, 256, 0, s>>>(T, c.hidden, c.top_k, static_cast<const uint16_t*>(yexp),
                                                  row_of, topk_w, static_cast<const uint16_t*>(yshared),

@@ -323,7 +323,9 @@ def test_grouped_gemm_f32(moe, orc):
 
 # ------------------------------------------------------------------ combine, bias update
 
-@pytest.mark.parametrize("mode,T,K,S", [("fp8", 300, 8, 1), ("fp8", 64, 1, 0), ("fp32", 64, 2, 1)])
+# BF16 rows: K = 4..8 take the kernel that issues every slot's load first, other K the general one
+@pytest.mark.parametrize("mode,T,K,S", [("fp8", 300, 8, 1), ("fp8", 64, 1, 0), ("fp32", 64, 2, 1),
+                                        ("fp8", 100, 6, 0), ("fp8", 70, 3, 1)])
 def test_combine_bitexact(moe, orc, mode, T, K, S):
     H = 7168 if mode == "fp8" else 256
     cfg = dict(hidden=H, inter=128, n_experts=16, n_group=4, topk_group=2, top_k=K,
