@@ -53,6 +53,7 @@ constexpr int kSfWarp0 = 4, kEpiWarp0 = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSfSlots = 16;                // K blocks of scale factors in TMEM
 constexpr int kSfCols = 16;                 // columns per slot: SFA at +0 (4), SFB at +8 (8)
+static_assert(kSfSlots % 4 == 0, "the scale writers fill four contiguous slots with one store");
 constexpr uint32_t kSfBase = 256;           // first scale-factor column
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kOutBox = 32 * 128;           // 32 rows x 128 B of BF16 output
@@ -105,6 +106,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
+}
+// Four consecutive 16-column groups in one store (columns taddr .. taddr + 63).
+__device__ __forceinline__ void tmem_st16x4(uint32_t taddr, const uint32_t (&v)[4][16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::"r"(taddr),
+                 "r"(v[0][0]), "r"(v[0][1]), "r"(v[0][2]), "r"(v[0][3]), "r"(v[0][4]), "r"(v[0][5]), "r"(v[0][6]), "r"(v[0][7]), "r"(v[0][8]), "r"(v[0][9]), "r"(v[0][10]), "r"(v[0][11]), "r"(v[0][12]), "r"(v[0][13]), "r"(v[0][14]), "r"(v[0][15]), "r"(v[1][0]), "r"(v[1][1]), "r"(v[1][2]), "r"(v[1][3]), "r"(v[1][4]), "r"(v[1][5]), "r"(v[1][6]), "r"(v[1][7]), "r"(v[1][8]), "r"(v[1][9]), "r"(v[1][10]), "r"(v[1][11]), "r"(v[1][12]), "r"(v[1][13]), "r"(v[1][14]), "r"(v[1][15]), "r"(v[2][0]), "r"(v[2][1]), "r"(v[2][2]), "r"(v[2][3]), "r"(v[2][4]), "r"(v[2][5]), "r"(v[2][6]), "r"(v[2][7]), "r"(v[2][8]), "r"(v[2][9]), "r"(v[2][10]), "r"(v[2][11]), "r"(v[2][12]), "r"(v[2][13]), "r"(v[2][14]), "r"(v[2][15]), "r"(v[3][0]), "r"(v[3][1]), "r"(v[3][2]), "r"(v[3][3]), "r"(v[3][4]), "r"(v[3][5]), "r"(v[3][6]), "r"(v[3][7]), "r"(v[3][8]), "r"(v[3][9]), "r"(v[3][10]), "r"(v[3][11]), "r"(v[3][12]), "r"(v[3][13]), "r"(v[3][14]), "r"(v[3][15])
+                 : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -281,6 +288,38 @@ grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                         a4[j] = __ldg(as_col + kb * kstep);
                         w0[j] = __ldg(ws0 + kb);
                         w1[j] = __ldg(ws1 + kb);
+                    }
+                    if (kb0 + 4 <= p.nkb && si % 4 == 0) {
+                        // the four slots si .. si+3 are contiguous: one 64-column store and one
+                        // wait for all four K blocks.  The MMA commits each slot's release in
+                        // K order, so the release of slot si+3 implies the other three.
+                        if (!__all_sync(0xffffffffu, mbar_wait(&sf_empty[si + 3], sph ^ 1u, abort_flag, kWaitBudget))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        uint32_t v[4][16];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t ea = ue8m0_of(a4[j]) * 0x01010101u;
+                            const uint32_t e0 = ue8m0_of(w0[j]) * 0x01010101u, e1 = ue8m0_of(w1[j]) * 0x01010101u;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                v[j][i] = ea;
+                                v[j][4 + i] = 0u;
+                                v[j][8 + i] = e0;
+                                v[j][12 + i] = e1;
+                            }
+                        }
+                        tmem_st16x4(lane_base + static_cast<uint32_t>(si * kSfCols), v);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            for (int j = 0; j < 4; ++j) mbar_arrive(&sf_full[si + j]);
+                        si += 4;
+                        if (si == kSfSlots) { si = 0; sph ^= 1u; }
+                        continue;
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
