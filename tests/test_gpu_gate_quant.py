@@ -84,3 +84,29 @@ def test_gate_quant_zero_tokens_and_unsupported(moe):
                            counts, torch.empty(4, 512, dtype=torch.uint8, device=DEV),
                            torch.empty(4, 4, device=DEV))
     assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("mode", ["fp8", "mxfp8"])
+def test_forward_is_the_same_across_the_fusion_threshold(moe, mode):
+    """moe_forward fuses the quantisation into the gate from MOE_GATE_QUANT_MIN_TOKENS tokens
+    up.  Every output row depends only on its own token, so the layer over that many tokens
+    (one fused kernel) and over one token fewer (the gate and the quantiser apart) must give
+    the shared tokens the same routing and the same output, bit for bit."""
+    from fp8_gemm_sigmoid_b300 import synthetic as sy
+    n = moe.MOE_GATE_QUANT_MIN_TOKENS
+    cfg = sy.config("v3_prefill", T=n, hidden=512, inter=256, n_experts=64, n_group=2, topk_group=1,
+                    top_k=4, mode=mode, seed=11)
+    inp = sy.make_inputs(cfg, DEV)
+    q = moe.quantize_weights(inp["W13"], inp["W2"], pow2=(mode == "mxfp8"))
+    w = dict(Wg=inp["Wg"].view(torch.uint16), **q)
+    res = []
+    for T in (n, n - 1):
+        out = moe.empty_outputs(cfg, T)
+        ws = moe.workspace(cfg, T)
+        moe.moe_forward(cfg, inp["x"][:T].view(torch.uint16), w, inp["bias"].clone(), 0,
+                        out["y"].view(torch.uint16), out["topk_idx"], out["topk_w"], out["counts"], ws)
+        torch.cuda.synchronize()
+        res.append({k: to_host(v)[: n - 1] for k, v in out.items() if k != "counts"})
+    assert moe.moe_device_error() == 0
+    for k in res[0]:
+        assert np.array_equal(res[0][k], res[1][k]), k
