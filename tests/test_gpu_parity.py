@@ -574,3 +574,30 @@ def test_gathered_gemm_equals_the_permuted_copy(moe, orc, mx):
     assert np.array_equal(outs[0][1], outs[1][1])
     unclaimed = to_host(perm_tok) < 0
     assert unclaimed.sum() == 2 and not outs[1][0][unclaimed].any()
+
+
+def test_forward_is_the_same_across_the_ring_depth_switch(moe, sy):
+    """The FP32-scale grouped GEMMs take a 4-stage operand ring (and store every down-GEMM row
+    directly) when the groups hold fewer than 64 rows on average, R < 64 * (E + 1).  Each
+    output element's sums run in the same order either way, and each output row depends only
+    on its own token, so the layer just above and just below the switch gives the shared tokens
+    the same routing and output, bit for bit."""
+    E, K = 64, 4
+    n = 64 * (E + 1) // (K + 1)          # T(K + 1) >= 64 (E + 1): the 3-stage ring
+    assert n * (K + 1) >= 64 * (E + 1) > (n - 1) * (K + 1)
+    cfg = sy.config("v3_prefill", T=n, hidden=512, inter=256, n_experts=E, n_group=2, topk_group=1,
+                    top_k=K, seed=12)
+    inp = sy.make_inputs(cfg, DEV)
+    q = moe.quantize_weights(inp["W13"], inp["W2"])
+    w = dict(Wg=inp["Wg"].view(torch.uint16), **q)
+    res = []
+    for T in (n, n - 1):
+        out = moe.empty_outputs(cfg, T)
+        ws = moe.workspace(cfg, T)
+        moe.moe_forward(cfg, inp["x"][:T].view(torch.uint16), w, inp["bias"].clone(), 0,
+                        out["y"].view(torch.uint16), out["topk_idx"], out["topk_w"], out["counts"], ws)
+        torch.cuda.synchronize()
+        res.append({k: to_host(v)[: n - 1] for k, v in out.items() if k != "counts"})
+    assert moe.moe_device_error() == 0
+    for k in res[0]:
+        assert np.array_equal(res[0][k], res[1][k]), k
