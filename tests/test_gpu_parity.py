@@ -601,3 +601,18 @@ def test_forward_is_the_same_across_the_ring_depth_switch(moe, sy):
     assert moe.moe_device_error() == 0
     for k in res[0]:
         assert np.array_equal(res[0][k], res[1][k]), k
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["v3_skewed", "v3_top1"])
+def test_forward_is_deterministic(moe, sy, v3, name):
+    """The layer at full size, run twice on the same inputs, gives the same bytes: routing,
+    weights, histogram, updated bias and output.  No atomic operation decides a value (the
+    histogram's atomic adds commute), and every sum has a fixed order.  The skewed workload
+    sends every token to one expert (the most contended histogram bin and the largest group);
+    the top-1 workload updates the bias."""
+    cfg = sy.config(name)
+    runs = [_run_forward(moe, sy, cfg, v3) for _ in range(2)]
+    for k in ("y", "topk_idx", "topk_w", "counts"):
+        assert np.array_equal(to_host(runs[0][1][k]), to_host(runs[1][1][k])), k
+    assert np.array_equal(to_host(runs[0][2]), to_host(runs[1][2]))  # the updated bias
