@@ -604,7 +604,7 @@ def test_forward_is_the_same_across_the_ring_depth_switch(moe, sy):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["v3_skewed", "v3_top1"])
+@pytest.mark.parametrize("name", ["v3_decode", "v3_skewed", "v3_top1"])
 def test_forward_is_deterministic(moe, sy, v3, name):
     """The layer at full size, run twice on the same inputs, gives the same bytes: routing,
     weights, histogram, updated bias and output.  No atomic operation decides a value (the
